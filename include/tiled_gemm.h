@@ -1,0 +1,163 @@
+/*
+ * tiled_gemm.h -- C ABI of the GB300 (sm_103a) output-stationary tiled GEMM.
+ *
+ * The operation is the matrix product of "Reading a matrix multiply through
+ * its tiles" (introduction): C = A @ B with A of shape M x K, B of shape
+ * K x N and C of shape M x N, C[i,j] = sum_k A[i,k] * B[k,j] ("Tiled Matrix
+ * Multiplication", idiomatic kernel notes: standard A x B, not A x B^T).  It
+ * is computed by the output-stationary loop nest of "Keep one output tile
+ * resident": every output tile keeps an FP32 accumulator resident while A
+ * and B tiles stream along K, and is written to C exactly once.
+ *
+ * Layout.  A, B and C are dense and row-major with leading dimensions K, N
+ * and N elements ("Tiled Matrix Multiplication", "Layout optimization": row-
+ * major for all tensors).  There are no strides and no transposes.  C must
+ * not overlap A or B.
+ *
+ * Memory and ownership.  A, B and C are device pointers owned by the caller
+ * (except where an entry point says "host").  The library allocates no
+ * device memory per call; its only state is one device status word per GPU
+ * and a cached driver entry point.
+ *
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ * default stream).  Calls are stream-ordered and asynchronous: they return
+ * after the launch, before the result is ready.
+ *
+ * Errors.  Every entry point returns a gemm_status_t; no C++ exception
+ * crosses this boundary.  Argument errors are detected on the host before
+ * anything is launched.  A device-side wait that runs out of its time budget
+ * is reported later by gemm_device_status().
+ */
+#ifndef TILED_GEMM_H
+#define TILED_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage / arithmetic types. */
+typedef enum {
+    GEMM_F32 = 0,  /* IEEE binary32 */
+    GEMM_F16 = 1,  /* IEEE binary16 */
+    GEMM_BF16 = 2  /* bfloat16 */
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1, /* null pointer where data is needed, negative or >= 2^31 size,
+                                   unknown enum value */
+    GEMM_ERR_UNSUPPORTED = 2,   /* valid but unsupported combination (types, or a forced
+                                   kernel whose alignment rules the operands break) */
+    GEMM_ERR_CUDA = 3,          /* a CUDA runtime call or the launch failed */
+    GEMM_ERR_TIMEOUT = 4        /* a bounded device-side wait ran out (see gemm_device_status) */
+} gemm_status_t;
+
+/* Kernel selection for gemm_ex_kernel. */
+typedef enum {
+    GEMM_KERNEL_AUTO = 0,      /* what gemm / gemm_ex use */
+    GEMM_KERNEL_SIMT = 1,      /* shared-memory tiled FFMA kernel, 64 x 64 x 16 tiles */
+    GEMM_KERNEL_SIMT_TPB3 = 2, /* the same kernel with 3 x 3 tiles, one thread per output
+                                  element ("Tiled Matrix Multiplication", TPB = 3) */
+    GEMM_KERNEL_TC_128x128 = 3,/* tcgen05, one CTA per 128 x 128 output tile */
+    GEMM_KERNEL_TC_128x256 = 4,/* tcgen05, one CTA per 128 x 256 output tile */
+    GEMM_KERNEL_TC_256x256 = 5 /* tcgen05 cta_group::2, one CTA pair per 256 x 256 tile */
+} gemm_kernel_t;
+
+/*
+ * gemm -- C = A @ B, written in acc_dtype.
+ *
+ * The result type equals the accumulator type, the convention of "Reading a
+ * matrix multiply through its tiles" ("Count the repeated reads" counts C at
+ * 4 bytes under FP32 accumulation).  in_dtype is the type of both A and B.
+ * Supported: (in, acc) = (F32, F32), (F16, F32), (BF16, F32).
+ *
+ * M == 0 or N == 0 is a no-op.  K == 0 writes zeros to C (the empty sum: the
+ * accumulator is initialised to zero and no K tile is added).
+ *
+ * Returns GEMM_OK, GEMM_ERR_INVALID_VALUE (a null A or B with K > 0 and
+ * M*N > 0, a null C with M*N > 0, a negative size or one >= 2^31, an unknown
+ * dtype), GEMM_ERR_UNSUPPORTED (another type combination) or GEMM_ERR_CUDA.
+ */
+int gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+         gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, void* stream);
+
+/*
+ * gemm_ex -- as gemm, with an explicit output type.
+ *
+ * The helion kernel of "Writing a matmul GPU kernel" accumulates in FP32 and
+ * stores into a tensor of the input dtype; out_dtype covers both that and the
+ * FP32 output of gemm.  The FP32 accumulator is converted to out_dtype with
+ * round-to-nearest-even (overflow to +-inf).  Supported (in, acc, out):
+ * (F32, F32, F32/F16/BF16) and (F16 or BF16, F32, F32/F16/BF16).
+ */
+int gemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+            gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
+            void* stream);
+
+/*
+ * gemm_ex_kernel -- as gemm_ex, with the kernel chosen by the caller.
+ *
+ * The tensor-core kernels need 16-bit inputs, 16-byte aligned A, B and C and
+ * row pitches (K and N elements of the input type, N of the output type) that
+ * are multiples of 16 bytes; a forced tensor-core kernel whose rules the
+ * operands break returns GEMM_ERR_UNSUPPORTED.  The SIMT kernels take any
+ * shape and any element-aligned pointer.  All kernels give results within
+ * the same accuracy bound; they differ in the order of the K summation.
+ */
+int gemm_ex_kernel(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                   gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
+                   gemm_kernel_t kernel, void* stream);
+
+/*
+ * gemm_select_kernel -- the kernel gemm_ex would launch for these arguments
+ * on the current device (a gemm_kernel_t), or a negative gemm_status_t when
+ * the arguments are invalid or unsupported.  Nothing is launched.
+ */
+int gemm_select_kernel(const void* A, const void* B, const void* C, int64_t M, int64_t N,
+                       int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                       gemm_dtype_t out_dtype);
+
+/*
+ * gemm_ex_host -- gemm_ex on HOST buffers, end to end.
+ *
+ * A_host (M x K), B_host (K x N) and C_host (M x N) are host buffers (pinned
+ * memory gives asynchronous copies; pageable memory works but the copies
+ * block).  dA, dB and dC are caller-owned device buffers of at least the same
+ * sizes.  On `stream` the call enqueues the host-to-device copies of A and B,
+ * the product, and the device-to-host copy of C; it returns after enqueueing
+ * (synchronize the stream before reading C_host).  Errors as gemm_ex.
+ */
+int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M, int64_t N,
+                 int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                 gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* stream);
+
+/*
+ * gemm_device_status -- synchronize `stream`, then read and clear the status
+ * word of the current device.  Returns GEMM_OK, GEMM_ERR_TIMEOUT if a
+ * tensor-core kernel launched since the last call gave up a bounded wait
+ * (its output is then incomplete), or GEMM_ERR_CUDA.
+ */
+int gemm_device_status(void* stream);
+
+/*
+ * gemm_debug_config -- test hook for the bounded-wait watchdog.
+ *
+ * wait_budget_cycles: SM clock cycles one device-side wait may take before
+ * the kernel gives up (<= 0 restores the default, about one second).
+ * fault_skip_kblock: when >= 0, the tensor-core producer skips the loads of
+ * that K step, so the MMA warp's wait on it runs out and the kernel returns
+ * GEMM_ERR_TIMEOUT through gemm_device_status; -1 (the default) disables it.
+ * The setting is process-wide.  Returns GEMM_OK.
+ */
+int gemm_debug_config(int64_t wait_budget_cycles, int fault_skip_kblock);
+
+/* gemm_error_string -- a static description of a gemm_status_t. */
+const char* gemm_error_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILED_GEMM_H */

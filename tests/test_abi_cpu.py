@@ -1,0 +1,70 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/tiled_gemm.h declares, and rejects bad arguments on the
+host before touching a device."""
+import ctypes
+
+import pytest
+
+import tiled_matrix_multiplication_output_gb300 as tg
+from tiled_matrix_multiplication_output_gb300 import build as tgbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if tgbuild.nvcc_path() is None:
+        pytest.skip("nvcc not available")
+    tgbuild.build()
+    return tg.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = tg.header_functions()
+    for n in ("gemm", "gemm_ex", "gemm_ex_kernel", "gemm_select_kernel", "gemm_ex_host",
+              "gemm_device_status", "gemm_debug_config", "gemm_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_header_symbol(lib):
+    raw = ctypes.CDLL(tg.library_path())
+    for name in tg.header_functions():
+        assert hasattr(raw, name), name
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    INV, UNS = tg.binding.ERR_INVALID_VALUE, tg.binding.ERR_UNSUPPORTED
+    p = 16  # a dummy non-null address; never dereferenced on these paths
+    assert tg.gemm(p, p, p, -1, 4, 4, tg.BF16, tg.F32) == INV
+    assert tg.gemm(p, p, p, 4, -1, 4, tg.BF16, tg.F32) == INV
+    assert tg.gemm(p, p, p, 4, 4, -1, tg.BF16, tg.F32) == INV
+    assert tg.gemm(p, p, p, 1 << 31, 4, 4, tg.BF16, tg.F32) == INV
+    assert tg.gemm(p, p, None, 4, 4, 4, tg.BF16, tg.F32) == INV       # null C
+    assert tg.gemm(None, p, p, 4, 4, 4, tg.BF16, tg.F32) == INV       # null A with K > 0
+    assert tg.gemm(p, p, p, 4, 4, 4, 7, tg.F32) == INV                # unknown dtype
+    assert tg.gemm_ex(p, p, p, 4, 4, 4, tg.BF16, tg.F32, 9) == INV
+    assert tg.gemm(p, p, p, 4, 4, 4, tg.BF16, tg.F16) == UNS          # FP16 accumulation
+    assert tg.gemm(p, p, p, 4, 4, 4, tg.F32, tg.BF16) == UNS
+    assert tg.gemm_ex_kernel(p, p, p, 4, 4, 4, tg.BF16, tg.F32, tg.F32, 42) == INV
+    assert tg.gemm_select_kernel(p, p, p, -3, 4, 4, tg.BF16, tg.F32, tg.F32) == -INV
+
+
+def test_empty_products_are_noops_without_a_device(lib):
+    assert tg.gemm(None, None, None, 0, 0, 0, tg.BF16, tg.F32) == 0
+    assert tg.gemm(None, None, None, 0, 17, 5, tg.F16, tg.F32) == 0
+    assert tg.gemm_ex(None, None, None, 9, 0, 5, tg.F32, tg.F32, tg.F32) == 0
+
+
+def test_error_strings(lib):
+    for code in range(5):
+        assert tg.error_string(code)
+    assert "unknown" in tg.error_string(99)
+
+
+def test_debug_config_roundtrip(lib):
+    assert tg.gemm_debug_config(1000, 3) == 0
+    assert tg.gemm_debug_config(0, -1) == 0
+
+
+def test_matmul_rejects_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        tg.matmul(torch.zeros(2, 2), torch.zeros(2, 2))

@@ -1,0 +1,194 @@
+"""ctypes binding of the C ABI in include/tiled_gemm.h.
+
+Argument marshalling only: every step of the product runs in the CUDA
+library.  The functions named like the C entry points take raw pointers
+(ints), sizes and enum values and return the C status code.  `matmul` is the
+convenience form for PyTorch CUDA tensors (PyTorch provides the device
+memory and the stream); it raises GemmError on a non-zero status.
+
+There is no fallback: if the library is missing or cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+F32, F16, BF16 = 0, 1, 2
+DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16}
+
+OK, ERR_INVALID_VALUE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+KERNELS = {
+    "auto": 0,
+    "simt": 1,
+    "simt_tpb3": 2,
+    "tc_128x128": 3,
+    "tc_128x256": 4,
+    "tc_256x256": 5,
+}
+KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
+
+HEADER = os.path.join(_build.ROOT, "include", "tiled_gemm.h")
+
+_lock = threading.Lock()
+_lib = None
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+_SIGNATURES = {
+    "gemm": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _p], _int),
+    "gemm_ex": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p], _int),
+    "gemm_ex_kernel": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _int, _p], _int),
+    "gemm_select_kernel": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int], _int),
+    "gemm_ex_host": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, _p, _p, _p], _int),
+    "gemm_device_status": ([_p], _int),
+    "gemm_debug_config": ([_i64, _int], _int),
+    "gemm_error_string": ([_int], ctypes.c_char_p),
+}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        super().__init__(f"{where}: status {code} ({error_string(code)})")
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/tiled_gemm.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load the CUDA library (optionally building it first)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if build_if_missing and not _build.up_to_date():
+                _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is not built; run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(path)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def gemm(A, B, C, M, N, K, in_dtype, acc_dtype, stream=None) -> int:
+    return load_library().gemm(A, B, C, M, N, K, in_dtype, acc_dtype, stream)
+
+
+def gemm_ex(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, stream=None) -> int:
+    return load_library().gemm_ex(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, stream)
+
+
+def gemm_ex_kernel(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, kernel, stream=None) -> int:
+    return load_library().gemm_ex_kernel(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype,
+                                         kernel, stream)
+
+
+def gemm_select_kernel(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype) -> int:
+    return load_library().gemm_select_kernel(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype)
+
+
+def gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype, dA, dB, dC,
+                 stream=None) -> int:
+    return load_library().gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype,
+                                       out_dtype, dA, dB, dC, stream)
+
+
+def gemm_device_status(stream=None) -> int:
+    return load_library().gemm_device_status(stream)
+
+
+def gemm_debug_config(wait_budget_cycles: int = 0, fault_skip_kblock: int = -1) -> int:
+    return load_library().gemm_debug_config(wait_budget_cycles, fault_skip_kblock)
+
+
+def error_string(code: int) -> str:
+    try:
+        return load_library().gemm_error_string(code).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+gemm_error_string = error_string
+
+
+# ------------------------------------------------------- PyTorch convenience
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(dt) -> int:
+    torch = _torch()
+    if isinstance(dt, str):
+        return DTYPE_CODES[dt]
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[dt]
+
+
+def torch_dtype(code_or_name):
+    torch = _torch()
+    if isinstance(code_or_name, str):
+        code_or_name = DTYPE_CODES[code_or_name]
+    return {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}[code_or_name]
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def matmul(A, B, out_dtype=None, kernel: str | int = "auto", out=None, stream=None):
+    """C = A @ B for contiguous row-major CUDA tensors (FP32 accumulation).
+
+    out_dtype defaults to FP32 (the accumulator type); `out` may supply a
+    preallocated contiguous (M, N) tensor of that type.  Runs on `stream`
+    (default: PyTorch's current stream) and returns without synchronizing.
+    """
+    torch = _torch()
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"bad shapes {tuple(A.shape)} @ {tuple(B.shape)}")
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous row-major")
+    M, K = A.shape
+    N = B.shape[1]
+    odt = torch.float32 if out_dtype is None else (
+        torch_dtype(out_dtype) if isinstance(out_dtype, (str, int)) else out_dtype)
+    if out is None:
+        out = torch.empty((M, N), dtype=odt, device=A.device)
+    elif out.shape != (M, N) or out.dtype != odt or not out.is_contiguous():
+        raise ValueError("out must be a contiguous (M, N) tensor of the output dtype")
+    kid = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+    rc = gemm_ex_kernel(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                        dtype_code(A.dtype), F32, dtype_code(odt), kid, _stream_handle(stream))
+    if rc != OK:
+        raise GemmError(rc, "gemm_ex_kernel")
+    return out

@@ -1,0 +1,280 @@
+// The C ABI declared in include/tiled_gemm.h: argument validation, kernel
+// selection, the device status word, and the host-buffer entry point.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "launch.h"
+#include "tc_params.h"
+#include "tiled_gemm.h"
+
+namespace tmmo {
+namespace {
+
+// One status word per device (the watchdog of the tensor-core kernel).
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultWaitBudget = 2000000000LL;  // ~1 s of SM clock
+
+std::atomic<long long> g_wait_budget{kDefaultWaitBudget};
+std::atomic<int> g_fault_skip_kblock{-1};
+
+struct DeviceInfo {
+    int num_sms = 0;
+    int* status = nullptr;
+    bool ready = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Set-up of the current device, once: SM count and the status word address.
+cudaError_t device_info(DeviceInfo* out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess)
+            return err;
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_status_word);
+        if (err != cudaSuccess)
+            return err;
+        d.status = static_cast<int*>(p);
+        d.ready = true;
+    }
+    *out = d;
+    return cudaSuccess;
+}
+
+bool valid_dtype(int dt) { return dt == GEMM_F32 || dt == GEMM_F16 || dt == GEMM_BF16; }
+int dt_size(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side argument check shared by every entry point.
+int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+             int in_dtype, int acc_dtype, int out_dtype)
+{
+    if (!valid_dtype(in_dtype) || !valid_dtype(acc_dtype) || !valid_dtype(out_dtype))
+        return GEMM_ERR_INVALID_VALUE;
+    const int64_t lim = int64_t(1) << 31;
+    if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
+        return GEMM_ERR_INVALID_VALUE;
+    if (M > 0 && N > 0) {
+        if (!C)
+            return GEMM_ERR_INVALID_VALUE;
+        if (K > 0 && (!A || !B))
+            return GEMM_ERR_INVALID_VALUE;
+    }
+    if (acc_dtype != GEMM_F32)
+        return GEMM_ERR_UNSUPPORTED;
+    return GEMM_OK;
+}
+
+// Whether a tensor-core kernel can take these operands: 16-bit inputs, FP32
+// accumulation, 16-byte aligned bases and row pitches (TMA rules).
+bool tc_eligible(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                 int in_dtype, int out_dtype)
+{
+    if (((M + 127) / 128) * ((N + 127) / 128) >= (int64_t(1) << 31))
+        return false;  // tile indices are 32-bit
+    if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16)
+        return false;
+    if (K <= 0)
+        return false;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C))
+        return false;
+    if ((K * dt_size(in_dtype)) % 16 != 0 || (N * dt_size(in_dtype)) % 16 != 0)
+        return false;
+    if ((N * dt_size(out_dtype)) % 16 != 0)
+        return false;
+    return true;
+}
+
+// The automatic choice.  Tiny products go to the SIMT kernel (a tensor-core
+// launch has a fixed set-up cost); otherwise the largest tile that still
+// gives every SM work.
+int auto_kernel(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                int in_dtype, int out_dtype, int num_sms)
+{
+    if (!tc_eligible(A, B, C, M, N, K, in_dtype, out_dtype))
+        return GEMM_KERNEL_SIMT;
+    const double flops = 2.0 * double(M) * double(N) * double(K);
+    if (flops < 2.0 * 64 * 64 * 64)
+        return GEMM_KERNEL_SIMT;
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    if (pair_tiles >= num_sms / 2)
+        return GEMM_KERNEL_TC_256x256;
+    const int64_t wide_tiles = ((M + 127) / 128) * ((N + 255) / 256);
+    if (wide_tiles >= num_sms)
+        return GEMM_KERNEL_TC_128x256;
+    return GEMM_KERNEL_TC_128x128;
+}
+
+int run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int in_dtype,
+        int acc_dtype, int out_dtype, int kernel, cudaStream_t stream)
+{
+    int rc = validate(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype);
+    if (rc != GEMM_OK)
+        return rc;
+    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_TC_256x256)
+        return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (kernel == GEMM_KERNEL_AUTO)
+        kernel = auto_kernel(A, B, C, M, N, K, in_dtype, out_dtype, d.num_sms);
+    if (kernel >= GEMM_KERNEL_TC_128x128) {
+        if (!tc_eligible(A, B, C, M, N, K, in_dtype, out_dtype))
+            return GEMM_ERR_UNSUPPORTED;
+        TcLaunch l{};
+        l.variant = kernel;
+        l.in_dtype = in_dtype;
+        l.out_dtype = out_dtype;
+        l.A = A;
+        l.B = B;
+        l.C = C;
+        l.M = static_cast<int>(M);
+        l.N = static_cast<int>(N);
+        l.K = static_cast<int>(K);
+        l.num_sms = d.num_sms;
+        l.status = d.status;
+        l.wait_budget = g_wait_budget.load();
+        l.fault_skip_kblock = g_fault_skip_kblock.load();
+        cudaError_t err = tc_gemm_launch(l, stream);
+        if (err == cudaErrorNotSupported)
+            return GEMM_ERR_UNSUPPORTED;
+        return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+    cudaError_t err = simt_gemm_launch(kernel == GEMM_KERNEL_SIMT_TPB3, in_dtype, out_dtype, A, B,
+                                       C, static_cast<int>(M), static_cast<int>(N),
+                                       static_cast<int>(K), d.num_sms, stream);
+    return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tmmo
+
+using namespace tmmo;
+
+extern "C" int gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                    gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, void* stream)
+{
+    return run(A, B, C, M, N, K, in_dtype, acc_dtype, acc_dtype, GEMM_KERNEL_AUTO,
+               static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                       gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
+                       void* stream)
+{
+    return run(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, GEMM_KERNEL_AUTO,
+               static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gemm_ex_kernel(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                              int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                              gemm_dtype_t out_dtype, gemm_kernel_t kernel, void* stream)
+{
+    return run(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, kernel,
+               static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gemm_select_kernel(const void* A, const void* B, const void* C, int64_t M,
+                                  int64_t N, int64_t K, gemm_dtype_t in_dtype,
+                                  gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype)
+{
+    int rc = validate(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype);
+    if (rc != GEMM_OK)
+        return -rc;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return -GEMM_ERR_CUDA;
+    return auto_kernel(A, B, C, M, N, K, in_dtype, out_dtype, d.num_sms);
+}
+
+extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
+                            int64_t N, int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                            gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* stream)
+{
+    int rc = validate(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype);
+    if (rc != GEMM_OK)
+        return rc;
+    rc = validate(dA, dB, dC, M, N, K, in_dtype, acc_dtype, out_dtype);
+    if (rc != GEMM_OK)
+        return rc;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t in_b = static_cast<size_t>(dt_size(in_dtype));
+    const size_t out_b = static_cast<size_t>(dt_size(out_dtype));
+    if (K > 0) {
+        if (cudaMemcpyAsync(dA, A_host, size_t(M) * size_t(K) * in_b, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(dB, B_host, size_t(K) * size_t(N) * in_b, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    rc = run(dA, dB, dC, M, N, K, in_dtype, acc_dtype, out_dtype, GEMM_KERNEL_AUTO, s);
+    if (rc != GEMM_OK)
+        return rc;
+    if (cudaMemcpyAsync(C_host, dC, size_t(M) * size_t(N) * out_b, cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+extern "C" int gemm_device_status(void* stream)
+{
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpy(&value, d.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(d.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+extern "C" int gemm_debug_config(int64_t wait_budget_cycles, int fault_skip_kblock)
+{
+    g_wait_budget.store(wait_budget_cycles > 0 ? wait_budget_cycles : kDefaultWaitBudget);
+    g_fault_skip_kblock.store(fault_skip_kblock >= 0 ? fault_skip_kblock : -1);
+    return GEMM_OK;
+}
+
+extern "C" const char* gemm_error_string(int status)
+{
+    switch (status) {
+    case GEMM_OK:
+        return "success";
+    case GEMM_ERR_INVALID_VALUE:
+        return "invalid argument (null pointer, negative or too large size, unknown enum)";
+    case GEMM_ERR_UNSUPPORTED:
+        return "unsupported type combination or operand alignment for the chosen kernel";
+    case GEMM_ERR_CUDA:
+        return "CUDA runtime error or launch failure";
+    case GEMM_ERR_TIMEOUT:
+        return "a device-side wait ran out of its time budget; the output is incomplete";
+    default:
+        return "unknown status";
+    }
+}

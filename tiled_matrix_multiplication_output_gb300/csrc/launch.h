@@ -1,0 +1,41 @@
+// Internal launchers behind the C ABI (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace tmmo {
+
+// Internal dtype codes; they match gemm_dtype_t.
+enum { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
+
+// Tensor-core kernel variants; they match the gemm_kernel_t values.
+enum { TC_128x128 = 3, TC_128x256 = 4, TC_256x256 = 5 };
+
+cudaError_t simt_gemm_launch(bool tpb3, int in_dtype, int out_dtype, const void* A, const void* B,
+                             void* C, int M, int N, int K, int num_sms, cudaStream_t stream);
+
+struct TcLaunch {
+    int variant;        // TC_128x128, TC_128x256 or TC_256x256
+    int in_dtype;       // DT_F16 or DT_BF16
+    int out_dtype;      // DT_F32, DT_F16 or DT_BF16
+    const void* A;
+    const void* B;
+    void* C;
+    int M, N, K;
+    int num_sms;
+    int* status;        // device status word
+    long long wait_budget;
+    int fault_skip_kblock;
+};
+
+// Encodes the tensor maps and launches; returns cudaSuccess, a CUDA error, or
+// cudaErrorNotSupported when the driver entry point for tensor maps is
+// unavailable.
+cudaError_t tc_gemm_launch(const TcLaunch& l, cudaStream_t stream);
+
+// Output tile of a tensor-core variant (rows x columns).
+void tc_tile_shape(int variant, int* tile_m, int* tile_n);
+
+}  // namespace tmmo

@@ -1,0 +1,176 @@
+// Shared-memory tiled SIMT GEMM: FP32 fused multiply-adds on the CUDA cores.
+//
+// This is the kernel shape of "Tiled Matrix Multiplication" (manual tiled
+// kernel): a thread block owns one BM x BN output tile, walks K in tiles of
+// BK, stages an A tile and a B tile in shared memory behind a barrier,
+// accumulates in registers, and writes its outputs once after the last K
+// tile.  K tiles are ceil(K / BK) with guarded loads (zero fill past the
+// edges, which adds exactly zero), so any M, N, K is exact, including the
+// partial tiles the pages' idiomatic kernel would drop.
+//
+// Differences from the page's kernel, for sm_103a:
+//  * each thread accumulates a TM x TN micro-tile (strided by the thread
+//    grid, so consecutive threads touch consecutive columns: conflict-free
+//    B reads and coalesced C writes); TM = TN = 1 with BM = BN = BK = 3 is
+//    exactly the page's TPB = 3, one-thread-per-output kernel;
+//  * the A tile is stored K-major in shared memory (As[k][m], padded by one
+//    word) so a warp's row reads are broadcasts and its tile stores are
+//    conflict-free -- the access pattern the page's bank-conflict note
+//    recommends;
+//  * inputs are widened to FP32 when staged, so FP32, FP16 and BF16 inputs
+//    share the kernel; the FP32 result is rounded to the output type with
+//    round-to-nearest-even;
+//  * the grid is 1-D and each block strides over output tiles, so any M, N
+//    fit the launch limits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "launch.h"
+
+namespace tmmo {
+namespace {
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__half* p, float v) { *p = __float2half_rn(v); }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+template <int BM, int BN, int BK, int TM, int TN, typename InT, typename OutT>
+__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+    simt_gemm_kernel(const InT* __restrict__ A, const InT* __restrict__ B, OutT* __restrict__ C,
+                     int M, int N, int K)
+{
+    constexpr int TX = BN / TN;  // threads along N
+    constexpr int TY = BM / TM;  // threads along M
+    constexpr int NT = TX * TY;
+    __shared__ float As[BK][BM + 1];
+    __shared__ float Bs[BK][BN + 1];
+
+    const int tid = threadIdx.x;
+    const int tx = tid % TX;
+    const int ty = tid / TX;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int tiles_m = (M + BM - 1) / BM;
+    const long long num_tiles = static_cast<long long>(tiles_m) * tiles_n;
+
+    for (long long tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int m0 = static_cast<int>(tile / tiles_n) * BM;
+        const int n0 = static_cast<int>(tile % tiles_n) * BN;
+
+        float acc[TM][TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+                acc[i][j] = 0.0f;
+
+        for (int k0 = 0; k0 < K; k0 += BK) {
+            // Stage the A tile (BM x BK): consecutive threads read
+            // consecutive k of one row (coalesced), stored K-major.
+            for (int e = tid; e < BM * BK; e += NT) {
+                const int i = e / BK, k = e % BK;
+                const int gm = m0 + i, gk = k0 + k;
+                As[k][i] = (gm < M && gk < K) ? to_f32(A[static_cast<long long>(gm) * K + gk]) : 0.0f;
+            }
+            // Stage the B tile (BK x BN): consecutive threads read
+            // consecutive columns of one row (coalesced).
+            for (int e = tid; e < BK * BN; e += NT) {
+                const int k = e / BN, j = e % BN;
+                const int gk = k0 + k, gn = n0 + j;
+                Bs[k][j] = (gk < K && gn < N) ? to_f32(B[static_cast<long long>(gk) * N + gn]) : 0.0f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < BK; ++k) {
+                float a[TM], b[TN];
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+                    a[i] = As[k][ty + i * TY];
+#pragma unroll
+                for (int j = 0; j < TN; ++j)
+                    b[j] = Bs[k][tx + j * TX];
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j)
+                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            }
+            __syncthreads();
+        }
+
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int gm = m0 + ty + i * TY;
+            if (gm >= M)
+                continue;
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const int gn = n0 + tx + j * TX;
+                if (gn < N)
+                    store_out(C + static_cast<long long>(gm) * N + gn, acc[i][j]);
+            }
+        }
+    }
+}
+
+template <int BM, int BN, int BK, int TM, int TN, typename InT, typename OutT>
+cudaError_t launch_simt(const void* A, const void* B, void* C, int M, int N, int K, int num_sms,
+                        cudaStream_t stream)
+{
+    constexpr int NT = (BM / TM) * (BN / TN);
+    const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    // Enough blocks for several resident per SM; each strides over tiles.
+    const long long cap = static_cast<long long>(std::max(num_sms, 1)) * 16;
+    const int grid = static_cast<int>(std::max<long long>(1, std::min(tiles, cap)));
+    simt_gemm_kernel<BM, BN, BK, TM, TN, InT, OutT><<<grid, NT, 0, stream>>>(
+        static_cast<const InT*>(A), static_cast<const InT*>(B), static_cast<OutT*>(C), M, N, K);
+    return cudaGetLastError();
+}
+
+template <int BM, int BN, int BK, int TM, int TN, typename InT>
+cudaError_t dispatch_out(int out_dtype, const void* A, const void* B, void* C, int M, int N,
+                         int K, int num_sms, cudaStream_t s)
+{
+    switch (out_dtype) {
+    case DT_F32:
+        return launch_simt<BM, BN, BK, TM, TN, InT, float>(A, B, C, M, N, K, num_sms, s);
+    case DT_F16:
+        return launch_simt<BM, BN, BK, TM, TN, InT, __half>(A, B, C, M, N, K, num_sms, s);
+    default:
+        return launch_simt<BM, BN, BK, TM, TN, InT, __nv_bfloat16>(A, B, C, M, N, K, num_sms, s);
+    }
+}
+
+template <int BM, int BN, int BK, int TM, int TN>
+cudaError_t dispatch_in(int in_dtype, int out_dtype, const void* A, const void* B, void* C, int M,
+                        int N, int K, int num_sms, cudaStream_t s)
+{
+    switch (in_dtype) {
+    case DT_F32:
+        return dispatch_out<BM, BN, BK, TM, TN, float>(out_dtype, A, B, C, M, N, K, num_sms, s);
+    case DT_F16:
+        return dispatch_out<BM, BN, BK, TM, TN, __half>(out_dtype, A, B, C, M, N, K, num_sms, s);
+    default:
+        return dispatch_out<BM, BN, BK, TM, TN, __nv_bfloat16>(out_dtype, A, B, C, M, N, K,
+                                                                num_sms, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t simt_gemm_launch(bool tpb3, int in_dtype, int out_dtype, const void* A, const void* B,
+                             void* C, int M, int N, int K, int num_sms, cudaStream_t stream)
+{
+    if (tpb3)
+        return dispatch_in<3, 3, 3, 1, 1>(in_dtype, out_dtype, A, B, C, M, N, K, num_sms, stream);
+    return dispatch_in<64, 64, 16, 4, 4>(in_dtype, out_dtype, A, B, C, M, N, K, num_sms, stream);
+}
+
+}  // namespace tmmo

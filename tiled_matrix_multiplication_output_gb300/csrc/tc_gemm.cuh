@@ -1,0 +1,454 @@
+// Output-stationary tiled C = A @ B on the 5th-generation tensor cores.
+//
+// The loop nest is the one of "Reading a matrix multiply through its tiles"
+// ("Keep one output tile resident"): for every output tile, the FP32
+// accumulator starts at zero, A and B tiles stream along K into fast memory
+// and are contracted into it, and the finished tile is written to C once.
+// On sm_103a that becomes:
+//
+//   * a persistent grid (one CTA, or one CTA pair, per SM) that strides over
+//     the output tiles in grouped raster order, so that concurrently running
+//     tiles share A row-panels and B column-panels in L2;
+//   * warp 0: the TMA producer.  It streams 128-byte-swizzled A boxes
+//     (128 rows x 64 K, K-major) and B boxes (64 K x 64 N, N-major, i.e. B
+//     stays row-major and is not transposed) into a STAGES-deep shared-memory
+//     ring guarded by full/empty mbarriers;
+//   * warp 1: the MMA issuer.  One thread issues tcgen05.mma (K = 16 per
+//     instruction, four per 64-wide K step) into an FP32 accumulator held in
+//     tensor memory (TMEM); the first MMA of a tile runs with accumulation
+//     disabled, which is the "zero the accumulator" step.  Two accumulators
+//     are kept so the epilogue of tile t overlaps the main loop of tile t+1;
+//   * warps 2-5: the epilogue.  Each warp owns 32 TMEM lanes (32 output
+//     rows), reads 32 columns at a time with tcgen05.ld, converts FP32 to the
+//     output type with round-to-nearest-even, writes a 128-byte-swizzled
+//     staging buffer and issues a TMA store.  The store clips rows >= M and
+//     columns >= N, and TMA loads fill out-of-range A/B elements with zeros
+//     (which add exactly nothing), so partial edge tiles in M, N and K are
+//     exact ("Edge tiles still matter").
+//
+// CG = 2 runs the same protocol on a CTA pair (cta_group::2): each CTA loads
+// its own 128 rows of A and half of the B columns, the leader CTA issues
+// M = 256 MMAs that read both CTAs' shared memory, and each CTA's TMEM holds
+// its 128 rows of the 256 x BN accumulator.  No TMA multicast is used.
+//
+// Every mbarrier wait is bounded by a clock budget.  When one runs out the
+// kernel records GEMM_ERR_TIMEOUT in the device status word, every role
+// leaves its loop, in-flight copies and MMAs are drained (again bounded),
+// TMEM is freed and the kernel returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "tc_params.h"
+
+namespace tmmo {
+
+constexpr int TC_BM = 128;       // accumulator rows per CTA (TMEM lanes)
+constexpr int TC_BK = 64;        // K per stage: 64 x 2 bytes = one 128-byte swizzle row
+constexpr int TC_UMMA_K = 16;    // K per tcgen05.mma for 16-bit inputs
+constexpr int TC_THREADS = 192;  // 6 warps
+constexpr int TC_EPI_WARP0 = 2;
+constexpr int TC_STAGING_BYTES = 4096;  // 32 rows x 128 bytes per warp buffer
+
+template <int CG, int BN, int STAGES>
+struct TcLayout {
+    static constexpr int A_STAGE = TC_BM * TC_BK * 2;            // 16 KiB
+    static constexpr int B_COLS = BN / CG;                       // B columns held per CTA
+    static constexpr int B_STAGE = TC_BK * B_COLS * 2;
+    static constexpr int B_BOXES = B_COLS / 64;                  // 64-column, 8 KiB boxes
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;        // bytes landing per CTA
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_STAGING = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_BAR = OFF_STAGING + 4 * 2 * TC_STAGING_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
+    static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+    static constexpr uint32_t TMEM_COLS = 2 * BN;    // two FP32 accumulators
+    static_assert(B_COLS % 64 == 0, "B boxes are 64 columns wide");
+    static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
+                      TMEM_COLS == 512,
+                  "TMEM allocations are a power of two >= 32 columns");
+    static_assert(SMEM_ALLOC <= 232448, "exceeds 227 KiB of dynamic shared memory");
+};
+
+// Instruction descriptor of tcgen05.mma kind::f16: F32 accumulator (bits
+// 4-5 = 1), A/B type F16 (0) or BF16 (1) in bits 7-9 / 10-12, A K-major
+// (bit 15 = 0), B N-major (bit 16 = 1), N >> 3 in bits 17-22 and M >> 4 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t tc_idesc(bool bf16, int m, int n)
+{
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | (0u << 15) |
+           (1u << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Grouped raster order: tiles are taken `group_m` tile-rows at a time and,
+// inside a group, down the rows of one tile-column before the next column.
+__device__ __forceinline__ void tc_tile_coords(int t, const TcParams& p, int& mb, int& nb)
+{
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.tiles_m - first_m, p.group_m);
+    const int r = t - g * per_group;
+    mb = first_m + r % gm;
+    nb = r / gm;
+}
+
+struct TcWatch {
+    volatile int* abort_flag;  // shared memory, this CTA
+    int* status;               // device status word
+    long long budget;          // clock cycles per wait
+};
+
+__device__ __forceinline__ void tc_raise(const TcWatch& w)
+{
+    *w.abort_flag = 1;
+    if (w.status)
+        atomicCAS(w.status, 0, TC_STATUS_TIMEOUT);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if the budget ran out
+// (and raises the abort) or another role already aborted.
+template <bool CLUSTER_SCOPE = false>
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const TcWatch& w)
+{
+    auto probe = [&]() {
+        return CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (probe())
+        return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (probe())
+            return true;
+        if (*w.abort_flag)
+            return false;
+        if (clock64() - t0 > w.budget) {
+            tc_raise(w);
+            return false;
+        }
+    }
+}
+
+template <typename OutT>
+struct TcOut;
+template <>
+struct TcOut<float> {
+    static constexpr int STRIP = 32;  // columns per 128-byte staging row
+};
+template <>
+struct TcOut<__half> {
+    static constexpr int STRIP = 64;
+};
+template <>
+struct TcOut<__nv_bfloat16> {
+    static constexpr int STRIP = 64;
+};
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __half*)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16*)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Read one 128-byte-wide strip (32 rows x STRIP columns) of the accumulator
+// from TMEM, convert, and write it to a swizzled staging buffer: 16-byte
+// chunk c of row r goes to chunk position c ^ (r % 8), the layout a
+// SWIZZLE_128B TMA store expects, and conflict-free for 8 rows at a time.
+template <typename OutT>
+__device__ __forceinline__ void tc_strip_to_smem(uint32_t taddr, uint32_t staging, uint32_t row)
+{
+    const uint32_t row_base = staging + row * 128;
+    const uint32_t sw = row & 7;
+    if constexpr (sizeof(OutT) == 4) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            st_shared_v4(row_base + ((c ^ sw) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                         v[4 * c + 3]);
+    } else {
+        uint32_t lo[32], hi[32];
+        tmem_ld_32x32b_x32(taddr, lo);
+        tmem_ld_32x32b_x32(taddr + 32, hi);
+        tmem_wait_ld();
+        OutT* tag = nullptr;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint32_t* src = (c < 4) ? lo : hi;
+            const int b = (c & 3) * 8;
+            uint32_t w0 = pack2(__uint_as_float(src[b + 0]), __uint_as_float(src[b + 1]), tag);
+            uint32_t w1 = pack2(__uint_as_float(src[b + 2]), __uint_as_float(src[b + 3]), tag);
+            uint32_t w2 = pack2(__uint_as_float(src[b + 4]), __uint_as_float(src[b + 5]), tag);
+            uint32_t w3 = pack2(__uint_as_float(src[b + 6]), __uint_as_float(src[b + 7]), tag);
+            st_shared_v4(row_base + ((c ^ sw) << 4), w0, w1, w2, w3);
+        }
+    }
+}
+
+template <int CG, int BN, int STAGES, typename OutT>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p)
+{
+    using L = TcLayout<CG, BN, STAGES>;
+    constexpr int STRIP = TcOut<OutT>::STRIP;
+    constexpr int TILE_M = TC_BM * CG;  // output rows per tile (per CTA pair)
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0;
+    const bool leader = (rank == 0);
+    const int unit = (CG == 2) ? (blockIdx.x >> 1) : blockIdx.x;   // CTA or CTA pair index
+    const int num_units = (CG == 2) ? (gridDim.x >> 1) : gridDim.x;
+    const TcWatch watch{abort_flag, p.status, p.wait_budget};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4 * CG);  // every epilogue warp of the pair
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before();
+    if constexpr (CG == 2)
+        cluster_sync();
+    else
+        __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t sA = sbase + L::OFF_A;
+            const uint32_t sB = sbase + L::OFF_B;
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s)
+                issued[s] = 0;
+            bool ok = true;
+            for (int t = unit; ok && t < p.num_tiles; t += num_units) {
+                int mb, nb;
+                tc_tile_coords(t, p, mb, nb);
+                const int a_row = mb * TILE_M + static_cast<int>(rank) * TC_BM;
+                const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!tc_wait(empty_bar(stage), phase ^ 1, watch)) {
+                        ok = false;
+                        break;
+                    }
+                    if (kb != p.fault_skip_kblock) {  // test hook: -1 in normal use
+                        const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+                        if (leader)
+                            mbar_arrive_expect_tx(full_bar(stage), CG * L::STAGE_BYTES);
+                        const uint32_t dA = sA + stage * L::A_STAGE;
+                        const uint32_t dB = sB + stage * L::B_STAGE;
+                        if constexpr (CG == 2) {
+                            tma_load_2d_pair(dA, &tmA, fb, kb * TC_BK, a_row);
+#pragma unroll
+                            for (int j = 0; j < L::B_BOXES; ++j)
+                                tma_load_2d_pair(dB + j * 8192, &tmB, fb, b_col + 64 * j, kb * TC_BK);
+                        } else {
+                            tma_load_2d(dA, &tmA, fb, kb * TC_BK, a_row);
+#pragma unroll
+                            for (int j = 0; j < L::B_BOXES; ++j)
+                                tma_load_2d(dB + j * 8192, &tmB, fb, b_col + 64 * j, kb * TC_BK);
+                        }
+                        ++issued[stage];
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok && leader) {
+                // Drain: wait (bounded) for the loads already issued into each
+                // stage of this CTA's barriers before shared memory goes away.
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued[s] == 0)
+                        continue;
+                    const uint32_t par = static_cast<uint32_t>(issued[s] - 1) & 1u;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(full_bar(s), par) && clock64() - t0 < p.wait_budget) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (leader && lane == 0) {
+            const uint32_t sA = sbase + L::OFF_A;
+            const uint32_t sB = sbase + L::OFF_B;
+            const uint32_t idesc = p.idesc;
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int t = unit; ok && t < p.num_tiles; t += num_units, ++local) {
+                const int acc = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!tc_wait<CG == 2>(tempty_bar(acc), acc_phase ^ 1, watch)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!tc_wait(full_bar(stage), phase, watch)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * L::A_STAGE;
+                    const uint32_t b0 = sB + stage * L::B_STAGE;
+#pragma unroll
+                    for (int k = 0; k < TC_BK / TC_UMMA_K; ++k) {
+                        // A: K-major rows of 128 bytes, 8-row groups 1024 bytes
+                        // apart; a K step of 16 moves 32 bytes along the row.
+                        const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 16, 1024);
+                        // B: N-major, 64-column atoms 8 KiB apart (LBO), 8-row
+                        // K groups 1024 bytes apart (SBO); 16 K rows = 2 KiB.
+                        const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, 8192, 1024);
+                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+                    }
+                    if constexpr (CG == 2)
+                        tc_commit_pair(empty_bar(stage), 0x3);
+                    else
+                        tc_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                if constexpr (CG == 2)
+                    tc_commit_pair(tfull_bar(acc), 0x3);
+                else
+                    tc_commit(tfull_bar(acc));
+            }
+            // Wait (bounded) until every MMA issued so far has completed, so
+            // TMEM and the input stages are no longer in use.
+            tc_commit_self<CG>(drain_bar);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < p.wait_budget) {
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const uint32_t staging0 =
+            sbase + L::OFF_STAGING + static_cast<uint32_t>((warp - TC_EPI_WARP0) * 2 * TC_STAGING_BYTES);
+        const uint32_t leader_tempty0 = (CG == 2) ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+        const uint32_t leader_tempty1 = (CG == 2) ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
+        int local = 0;
+        uint32_t buf = 0;
+        for (int t = unit; t < p.num_tiles; t += num_units, ++local) {
+            int mb, nb;
+            tc_tile_coords(t, p, mb, nb);
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            int ok = 1;
+            if (lane == 0)
+                ok = tc_wait(tfull_bar(acc), acc_phase, watch) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const int row0 = mb * TILE_M + static_cast<int>(rank) * TC_BM + q * 32;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int s = 0; s < BN / STRIP; ++s) {
+                const uint32_t stg = staging0 + buf * TC_STAGING_BYTES;
+                tc_strip_to_smem<OutT>(t_row + s * STRIP, stg, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int col0 = nb * BN + s * STRIP;
+                if (lane == 0 && row0 < p.M && col0 < p.N) {  // boxes wholly outside C write nothing
+                    tma_store_2d(&tmC, stg, col0, row0);
+                    bulk_commit_group();
+                    bulk_wait_group_read<1>();  // the other buffer is free again
+                }
+                __syncwarp();
+                buf ^= 1;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t tb = acc ? leader_tempty1 : leader_tempty0;
+                if constexpr (CG == 2)
+                    mbar_arrive_cluster(tb);
+                else
+                    mbar_arrive(tb);
+            }
+        }
+        if (lane == 0)
+            bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------- teardown
+    __syncwarp();  // reconverge each warp after its role's divergent loop
+    tc_fence_before();
+    if constexpr (CG == 2)
+        cluster_sync();
+    else
+        __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc<CG>(tmem_base, L::TMEM_COLS);
+    }
+}
+
+}  // namespace tmmo

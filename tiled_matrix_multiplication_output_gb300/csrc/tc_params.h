@@ -1,0 +1,22 @@
+// Launch parameters shared by the host dispatcher and the tensor-core kernel.
+#pragma once
+
+#include <cstdint>
+
+namespace tmmo {
+
+// Value written to the device status word when a bounded wait runs out.
+constexpr int TC_STATUS_TIMEOUT = 1;
+
+struct TcParams {
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles;  // output tiles of (128 * CG) x BN
+    int k_blocks;                      // ceil(K / 64)
+    int group_m;                       // raster group height, in tile rows
+    uint32_t idesc;                    // tcgen05 instruction descriptor
+    int* status;                       // device status word (never null)
+    long long wait_budget;             // clock cycles a single wait may take
+    int fault_skip_kblock;             // test hook: K step whose loads are skipped; -1 = none
+};
+
+}  // namespace tmmo
