@@ -1,0 +1,418 @@
+"""Benchmark of the output-stationary tiled GEMM on GB300.
+
+One step is one C = A @ B of the chosen workload (default: 8192^3, BF16
+inputs N(0,1)/sqrt(K), FP32 accumulation, BF16 output) through the C ABI,
+with A and B resident in HBM.  A + B + C take 384 MiB, more than the 129 MB
+L2, so consecutive steps cannot reuse inputs from L2.
+
+Prints ONE JSON line (rank 0).  Keys beyond the common ones:
+  roofline      dominant kernel vs the measured dense BF16 tensor peak
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+  e2e           the same metric through gemm_ex_host with pinned host
+                buffers (host-to-device copies of A, B and the device-to-host
+                copy of C inside the timed region)
+  clocks        SM clocks and throttle reasons sampled during the timed loop
+
+`--impl reference` times the CPU oracle instead (the only comparison arm:
+the pages publish no implementation).  With --gpus N > 1 (under torchrun)
+each rank runs an independent replica of the workload (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (1×GB300) and % of dense FP16/BF16 tensor peak, vs CPU oracle"
+UNIT = "TFLOP/s"
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "tiled_matrix_multiplication_output_gb300", "csrc")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="square_8192_bf16")
+    ap.add_argument("--kernel", default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time only the GEMM launches (no e2e, cuBLAS context or CPU "
+                         "baseline); used for profiler captures")
+    return ap.parse_args()
+
+
+def source_digest() -> str:
+    """SHA-256 over the CUDA sources: ties committed ncu counters to the
+    kernel they were taken from."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def committed_traffic(kernel_name: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel
+    and workload, or None if absent or taken from different sources."""
+    path = os.path.join(PROFILES, f"{kernel_name}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256") != source_digest():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons (every 200 ms)."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.strip().split(",") for r in f if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_rate(A, B, target_seconds: float):
+    """Time the CPU oracle on a bounded sample: the first R rows of C
+    (R * N * K multiply-adds), R calibrated to about target_seconds.
+    Returns (TFLOP/s, rows, seconds, threads)."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    N = B.shape[1]
+    K = A.shape[1]
+    rows = max(1, min(threads, A.shape[0]))
+    t0 = time.perf_counter()
+    oracle.gemm(A[:rows], B, nthreads=threads)
+    dt = time.perf_counter() - t0
+    rate_rows = rows / max(dt, 1e-9)
+    rows = int(max(1, min(A.shape[0], rate_rows * target_seconds)))
+    t0 = time.perf_counter()
+    oracle.gemm(A[:rows], B, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K
+    return flops / dt / 1e12, rows, dt, min(threads, rows)
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the comparison arm: each step is a bounded sample
+    (whole rows of C) of the same workload."""
+    from tiled_matrix_multiplication_output_gb300 import inputs
+    import oracle
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    A, B = inputs.make(w)
+    oracle.build()
+    threads = os.cpu_count() or 1
+    # calibrate rows per step so warmup + steps take about two minutes
+    t0 = time.perf_counter()
+    probe_rows = max(1, min(threads, w.M))
+    oracle.gemm(A[:probe_rows], B, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.M, budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle.gemm(A[:rows], B, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(A[:rows], B, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    sample = (f"{rows} of {w.M} rows of C per step ({rows}x{w.N}x{w.K}), "
+              f"FP64 i-k-j loop over the rounded inputs")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, "cpu_oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(threads, rows),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, kernel):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in_dtype": w.in_dtype,
+            "acc_dtype": "f32", "out_dtype": w.out_dtype, "layout": "row-major A, B, C",
+            "kernel": kernel, "dist": w.dist, "seed": w.seed,
+            "l2": "A+B+C larger than L2" if (w.M * w.K + w.K * w.N) * 2 + w.M * w.N * 2 > 129e6
+            else "inputs smaller than L2 (small workload)"}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import tiled_matrix_multiplication_output_gb300 as tg
+    from tiled_matrix_multiplication_output_gb300 import binding, inputs
+
+    tg.load_library(build_if_missing=True)
+    w = inputs.WORKLOADS[args.workload]
+    A_cpu, B_cpu = inputs.make(w)
+    dev = torch.device("cuda", local)
+    A = A_cpu.to(dev)
+    B = B_cpu.to(dev)
+    odt = binding.torch_dtype(w.out_dtype)
+    C = torch.empty((w.M, w.N), dtype=odt, device=dev)
+    in_code = binding.dtype_code(w.in_dtype)
+    out_code = binding.dtype_code(w.out_dtype)
+    kid = tg.KERNELS[args.kernel]
+    chosen = kid if kid != 0 else tg.gemm_select_kernel(
+        A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, in_code, tg.F32, out_code)
+    kname = tg.KERNEL_NAMES.get(chosen, str(chosen))
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step():
+        rc = tg.gemm_ex_kernel(A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K,
+                               in_code, tg.F32, out_code, chosen, sh)
+        if rc != 0:
+            raise tg.GemmError(rc, "gemm_ex_kernel")
+
+    for _ in range(args.warmup if args.kernel_only else max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    rc = tg.gemm_device_status(sh)
+    if rc != 0:
+        raise tg.GemmError(rc, "warm-up")
+
+    # ---- timed region: K steps, events around every launch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.25)
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    total_ms = ev[0].elapsed_time(ev[-1])
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    rc = tg.gemm_device_status(sh)
+    if rc != 0:
+        raise tg.GemmError(rc, "timed region")
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    flops = float(w.flops)
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+
+    if args.kernel_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": ms_per_step, "config": config_of(w, kname),
+                              "gpu_launches": args.steps, "kernel_only": True}), flush=True)
+        return
+
+    # ---- end to end through the host-buffer entry point
+    in_b = 4 if w.in_dtype == "f32" else 2
+    out_b = 4 if w.out_dtype == "f32" else 2
+    Ah = A_cpu.pin_memory()
+    Bh = B_cpu.pin_memory()
+    Ch = torch.empty((w.M, w.N), dtype=odt).pin_memory()
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+
+    def host_step():
+        rc = tg.gemm_ex_host(Ah.data_ptr(), Bh.data_ptr(), Ch.data_ptr(), w.M, w.N, w.K,
+                             in_code, tg.F32, out_code, A.data_ptr(), B.data_ptr(),
+                             C.data_ptr(), sh)
+        if rc != 0:
+            raise tg.GemmError(rc, "gemm_ex_host")
+
+    for _ in range(3):
+        host_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        host_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    # ---- cuBLAS on the same inputs, as context only
+    for _ in range(5):
+        torch.matmul(A, B)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    n_cublas = 50
+    c0.record(stream)
+    for _ in range(n_cublas):
+        torch.matmul(A, B)
+    c1.record(stream)
+    torch.cuda.synchronize(dev)
+    cublas_tflops = flops * n_cublas / (c0.elapsed_time(c1) * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    avg_launch_ms = statistics.mean(per_launch)
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = committed_traffic(f"tc_gemm_{kname[3:]}" if kname.startswith("tc_") else kname,
+                                w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.in_dtype, "data": "synthetic",
+        "config": config_of(w, kname),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                     "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"])},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": (w.M * w.K + w.K * w.N) * in_b,
+                "d2h_bytes_per_step": w.M * w.N * out_b, "steps": e2e_steps,
+                "entry_point": "gemm_ex_host (pinned host buffers)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "context": {"cublas_torch_matmul_tflops": cublas_tflops,
+                    "per_launch_ms_min": min(per_launch), "per_launch_ms_median":
+                    statistics.median(per_launch)},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        v, rows, secs, cores = cpu_oracle_rate(A_cpu, B_cpu, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} of {w.M} rows of C ({rows}x{w.N}x{w.K}), {secs:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, rank, world_env)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -409,17 +409,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                    static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
             for (int s = 0; s < BN / STRIP; ++s) {
+                const int col0 = nb * BN + s * STRIP;
+                if (row0 >= p.M || col0 >= p.N)
+                    break;  // the rest of this warp's strips lie wholly outside C
                 const uint32_t stg = staging0 + buf * TC_STAGING_BYTES;
+                // This buffer is free once at most one store group (the one
+                // reading the other buffer) is still pending.
+                if (lane == 0)
+                    bulk_wait_group_read<1>();
+                __syncwarp();
                 tc_strip_to_smem<OutT>(t_row + s * STRIP, stg, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
-                const int col0 = nb * BN + s * STRIP;
-                if (lane == 0 && row0 < p.M && col0 < p.N) {  // boxes wholly outside C write nothing
+                if (lane == 0) {
                     tma_store_2d(&tmC, stg, col0, row0);
                     bulk_commit_group();
-                    bulk_wait_group_read<1>();  // the other buffer is free again
                 }
-                __syncwarp();
                 buf ^= 1;
             }
             tc_fence_before();
