@@ -356,7 +356,7 @@ def run_ours(args, rank, world, local):
         torch.matmul(A, B)
     c0 = torch.cuda.Event(enable_timing=True)
     c1 = torch.cuda.Event(enable_timing=True)
-    n_cublas = 50
+    n_cublas = args.steps   # same length as our timed loop, so both run at sustained clocks
     c0.record(stream)
     for _ in range(n_cublas):
         torch.matmul(A, B)

@@ -133,6 +133,17 @@ def test_entries_match_full_product():
     np.testing.assert_array_equal(va, Cabs[rows, cols])
 
 
+def test_entries_closed_form_worked_example():
+    A, B = load_worked_9x9()
+    rows = np.array([0, 8, 8, 3, 1])
+    cols = np.array([0, 8, 0, 5, 1])
+    v, va = oracle.gemm_entries(torch.tensor(A, dtype=torch.float32),
+                                torch.tensor(B, dtype=torch.float32), rows, cols)
+    want = [5832 * i + 162 * i * j + 72 * j + 3672 for i, j in zip(rows, cols)]
+    np.testing.assert_array_equal(v, want)
+    np.testing.assert_array_equal(va, want)
+
+
 def test_thread_count_does_not_change_result():
     A, B = inputs.draw(31, 29, 77, "f16", "uniform", seed=9)
     C1, _ = oracle.gemm(A, B, nthreads=1)
