@@ -10,6 +10,15 @@
 #include "launch.h"
 #include "tc_gemm.cuh"
 
+// Schedule and pipeline-depth choices, measured on GB300 (overridable at
+// build time for tuning sweeps).
+#ifndef TMMO_RASTER_GROUP
+#define TMMO_RASTER_GROUP 8  // tile rows per raster group
+#endif
+#ifndef TMMO_PAIR_STAGES
+#define TMMO_PAIR_STAGES 6   // shared-memory stages of the CTA-pair kernel
+#endif
+
 namespace tmmo {
 namespace {
 
@@ -128,7 +137,7 @@ cudaError_t launch_variant(const TcLaunch& l, cudaStream_t stream)
     p.tiles_n = (l.N + BN - 1) / BN;
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_blocks = (l.K + TC_BK - 1) / TC_BK;
-    p.group_m = 8;
+    p.group_m = TMMO_RASTER_GROUP;
     p.idesc = tc_idesc(l.in_dtype == DT_BF16, TC_BM * CG, BN);
     p.status = l.status;
     p.wait_budget = l.wait_budget;
@@ -194,7 +203,7 @@ cudaError_t tc_gemm_launch(const TcLaunch& l, cudaStream_t stream)
     case TC_128x256:
         return launch_out<1, 256, 4>(l, stream);
     case TC_256x256:
-        return launch_out<2, 256, 6>(l, stream);
+        return launch_out<2, 256, TMMO_PAIR_STAGES>(l, stream);
     default:
         return cudaErrorInvalidValue;
     }
