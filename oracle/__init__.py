@@ -62,6 +62,9 @@ def _load():
             lib.orc_gemm.argtypes = [_p, _p, ctypes.c_int, _i64, _i64, _i64, _p, _p, ctypes.c_int]
             lib.orc_gemm_entries.argtypes = [_p, _p, ctypes.c_int, _i64, _i64, _i64,
                                              _p, _p, _i64, _p, _p]
+            lib.orc_gemm_general.argtypes = [_p, _p, ctypes.c_int, _i64, _i64, _i64,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                             ctypes.c_double, _p, ctypes.c_int, _p, _p]
             lib.orc_tile_ranges.argtypes = [_i64, _i64, _p, _p, _i64]
             lib.orc_tile_ranges.restype = _i64
             lib.orc_traffic.argtypes = [_i64] * 9 + [_p]
@@ -129,6 +132,36 @@ def gemm(A: torch.Tensor, B: torch.Tensor, nthreads: int | None = None):
         nthreads = os.cpu_count() or 1
     rc = _load().orc_gemm(_ptr(a), _ptr(b), _DTYPE_CODE[A.dtype], M, N, K,
                           _ptr(C), _ptr(Cabs), int(nthreads))
+    assert rc == 0, rc
+    return C, Cabs
+
+
+def gemm_general(A: torch.Tensor, B: torch.Tensor, op_a: str = "n", op_b: str = "n",
+                 alpha: float = 1.0, beta: float = 0.0, C_in: torch.Tensor | None = None):
+    """(C, Cabs) in FP64 for C = alpha * op(A) @ op(B) + beta * C_in.
+
+    op "n" uses a matrix as stored; "t" its transpose (A stored K x M, B
+    stored N x K).  Cabs = |alpha| * sum_k |op(A)[i,k] op(B)[k,j]|."""
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must share a storage type")
+    ta, tb = op_a.lower() == "t", op_b.lower() == "t"
+    M, K = (A.shape[1], A.shape[0]) if ta else (A.shape[0], A.shape[1])
+    K2, N = (B.shape[1], B.shape[0]) if tb else (B.shape[0], B.shape[1])
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    a, b = _raw(A), _raw(B)
+    if C_in is not None:
+        c_in = _raw(C_in)
+        c_code = _DTYPE_CODE[C_in.dtype]
+        if tuple(C_in.shape) != (M, N):
+            raise ValueError("C_in must be M x N")
+    else:
+        c_in, c_code = np.zeros(0, dtype=np.float32), 0
+    C = np.empty((M, N), dtype=np.float64)
+    Cabs = np.empty((M, N), dtype=np.float64)
+    rc = _load().orc_gemm_general(_ptr(a), _ptr(b), _DTYPE_CODE[A.dtype], M, N, K, int(ta),
+                                  int(tb), float(alpha), float(beta), _ptr(c_in), c_code,
+                                  _ptr(C), _ptr(Cabs))
     assert rc == 0, rc
     return C, Cabs
 

@@ -270,6 +270,51 @@ int orc_gemm(const void *A, const void *B, int dtype, int64_t M, int64_t N,
     return rc;
 }
 
+/* The general form: C = alpha * op(A) @ op(B) + beta * C_in, where op(A) is
+ * M x K and op(B) is K x N.  op = 0 takes the matrix as stored (A row-major
+ * M x K, B row-major K x N); op = 1 takes its transpose (A stored row-major
+ * K x M, B stored row-major N x K), the transposed loadings the puzzle page
+ * lists for pre-transposed inputs ("Tiled Matrix Multiplication",
+ * "Educational: When would transposed loading be useful?").  C_in (storage
+ * type c_dtype, row-major M x N) is read only when beta != 0, the
+ * accumulate-into-the-output form of torch.addmm that the helion kernel
+ * builds its tiles with ("Writing a matmul GPU kernel").  Cabs receives
+ * |alpha| * sum_k |op(A)[i,k] op(B)[k,j]|.  Single-threaded, row by row. */
+int orc_gemm_general(const void *A, const void *B, int dtype, int64_t M, int64_t N, int64_t K,
+                     int op_a, int op_b, double alpha, double beta, const void *C_in,
+                     int c_dtype, double *C, double *Cabs)
+{
+    if (!dtype_ok(dtype) || !dtype_ok(c_dtype) || M < 0 || N < 0 || K < 0)
+        return -1;
+    if ((op_a != 0 && op_a != 1) || (op_b != 0 && op_b != 1))
+        return -1;
+    if (M * N > 0 && !C)
+        return -1;
+    if (M * N > 0 && K > 0 && (!A || !B))
+        return -1;
+    if (M * N > 0 && beta != 0.0 && !C_in)
+        return -1;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0, acc_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                int64_t ia = op_a ? k * M + i : i * K + k;
+                int64_t ib = op_b ? j * K + k : k * N + j;
+                double prod = load_elem(A, dtype, ia) * load_elem(B, dtype, ib);
+                acc += prod;
+                acc_abs += fabs(prod);
+            }
+            double c = alpha * acc;
+            if (beta != 0.0)
+                c += beta * load_elem(C_in, c_dtype, i * N + j);
+            C[i * N + j] = c;
+            if (Cabs)
+                Cabs[i * N + j] = fabs(alpha) * acc_abs;
+        }
+    }
+    return 0;
+}
+
 /* Selected entries C[rows[s], cols[s]], each a single k-ascending dot
  * product; used where the full product is too large to form on the host. */
 int orc_gemm_entries(const void *A, const void *B, int dtype, int64_t M,

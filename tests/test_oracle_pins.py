@@ -310,3 +310,49 @@ def test_tile_ranges_cover_exactly():
         assert sum(b - a for a, b in r) == n
         assert all(r[i][1] == r[i + 1][0] for i in range(len(r) - 1))
         assert all(0 < b - a <= t for a, b in r)
+
+
+# ------------------------------------------- transposed operands and addmm
+
+@pytest.mark.parametrize("op_a,op_b", [("n", "n"), ("t", "n"), ("n", "t"), ("t", "t")])
+def test_general_transposes_against_integer_loop(op_a, op_b):
+    """op(A) @ op(B) with the stored matrices transposed as the op says, on
+    integer inputs, against the pure-Python integer loop."""
+    for trial, (M, N, K) in enumerate([(5, 7, 3), (17, 9, 33), (1, 13, 8), (12, 1, 1)]):
+        A0, B0 = inputs.draw(M, N, K, "bf16", "int", seed=40 + trial)   # A0: M x K, B0: K x N
+        A = A0.t().contiguous() if op_a == "t" else A0
+        B = B0.t().contiguous() if op_b == "t" else B0
+        C, Cabs = oracle.gemm_general(A, B, op_a, op_b)
+        Ai, Bi = A0.to(torch.int64).tolist(), B0.to(torch.int64).tolist()
+        np.testing.assert_array_equal(C, np.array(_int_loop(Ai, Bi), dtype=np.float64))
+        C2, _ = oracle.gemm(A0, B0)
+        np.testing.assert_array_equal(C, C2)
+
+
+def test_general_transpose_is_not_identity():
+    """A non-square case where the transposed read differs from the plain one."""
+    A = torch.tensor([[1., 2.], [3., 4.], [5., 6.]])   # stored 3 x 2
+    B = torch.tensor([[1., 0., 2.], [0., 1., 3.]])      # stored 2 x 3
+    C_nn, _ = oracle.gemm_general(A, B, "n", "n")       # (3x2)(2x3)
+    np.testing.assert_array_equal(C_nn, [[1, 2, 8], [3, 4, 18], [5, 6, 28]])
+    C_tt, _ = oracle.gemm_general(A, B, "t", "t")       # (2x3)(3x2)
+    np.testing.assert_array_equal(C_tt, [[11, 18], [14, 22]])
+
+
+def test_general_alpha_beta_addmm():
+    """alpha * A @ B + beta * C_in on integers, exact; beta = 0 ignores C_in
+    (even NaN); A = 0 leaves beta * C_in."""
+    A, B = inputs.draw(9, 11, 7, "f16", "int", seed=50)
+    Cin = torch.randint(-9, 10, (9, 11), generator=torch.Generator().manual_seed(3)).to(torch.float32)
+    C, Cabs = oracle.gemm_general(A, B, alpha=2.0, beta=-3.0, C_in=Cin)
+    want = 2 * np.array(_int_loop(A.to(torch.int64).tolist(), B.to(torch.int64).tolist())) \
+        - 3 * Cin.numpy().astype(np.int64)
+    np.testing.assert_array_equal(C, want)
+    plain, plain_abs = oracle.gemm(A, B)
+    np.testing.assert_array_equal(Cabs, 2 * plain_abs)
+    nan_in = torch.full((9, 11), float("nan"))
+    C0, _ = oracle.gemm_general(A, B, beta=0.0, C_in=nan_in)
+    np.testing.assert_array_equal(C0, plain)
+    Z = torch.zeros_like(A)
+    Cz, _ = oracle.gemm_general(Z, B, alpha=5.0, beta=0.5, C_in=Cin)
+    np.testing.assert_array_equal(Cz, 0.5 * Cin.numpy())
