@@ -11,8 +11,8 @@
  *
  * Layout.  A, B and C are dense and row-major with leading dimensions K, N
  * and N elements ("Tiled Matrix Multiplication", "Layout optimization": row-
- * major for all tensors).  There are no strides and no transposes.  C must
- * not overlap A or B.
+ * major for all tensors); gemm_general also takes A or B stored transposed.
+ * There are no other strides.  C must not overlap A or B.
  *
  * Memory and ownership.  A, B and C are device pointers owned by the caller
  * (except where an entry point says "host").  The library allocates no
@@ -54,7 +54,13 @@ typedef enum {
     GEMM_ERR_TIMEOUT = 4        /* a bounded device-side wait ran out (see gemm_device_status) */
 } gemm_status_t;
 
-/* Kernel selection for gemm_ex_kernel. */
+/* Operand form for gemm_general. */
+typedef enum {
+    GEMM_OP_N = 0, /* the matrix as stored: A row-major M x K, B row-major K x N */
+    GEMM_OP_T = 1  /* its transpose: A stored row-major K x M, B stored row-major N x K */
+} gemm_op_t;
+
+/* Kernel selection for gemm_ex_kernel and gemm_general. */
 typedef enum {
     GEMM_KERNEL_AUTO = 0,      /* what gemm / gemm_ex use */
     GEMM_KERNEL_SIMT = 1,      /* shared-memory tiled FFMA kernel, 64 x 64 x 16 tiles */
@@ -109,6 +115,31 @@ int gemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t
 int gemm_ex_kernel(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                    gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
                    gemm_kernel_t kernel, void* stream);
+
+/*
+ * gemm_general -- C = alpha * op(A) @ op(B) + beta * C.
+ *
+ * op(A) is M x K and op(B) is K x N.  GEMM_OP_N uses an operand as stored;
+ * GEMM_OP_T uses its transpose, i.e. A is stored row-major K x M or B is
+ * stored row-major N x K -- the pre-transposed inputs of "Tiled Matrix
+ * Multiplication" ("When would transposed loading be useful?"); the kernels
+ * read them in place through the matching tile layout, nothing is
+ * transposed in memory.  beta != 0 reads C (row-major M x N, out_dtype)
+ * before it is overwritten -- the accumulate-into-C form of torch.addmm that
+ * the helion kernel of "Writing a matmul GPU kernel" builds its tiles with;
+ * beta == 0 never reads C.  alpha and beta are applied in FP32 to the FP32
+ * accumulator before the conversion to out_dtype.  C must not overlap A or B.
+ *
+ * The tensor-core kernels need the row pitches of A and B as stored (K or M,
+ * N or K elements) and of C (N) to be multiples of 16 bytes; otherwise the
+ * automatic choice is the SIMT kernel.  Types, sizes, K == 0 (C = beta * C)
+ * and errors as gemm_ex_kernel, plus GEMM_ERR_INVALID_VALUE for an unknown
+ * gemm_op_t.
+ */
+int gemm_general(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                 gemm_op_t op_a, gemm_op_t op_b, float alpha, float beta, gemm_dtype_t in_dtype,
+                 gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype, gemm_kernel_t kernel,
+                 void* stream);
 
 /*
  * gemm_select_kernel -- the kernel gemm_ex would launch for these arguments

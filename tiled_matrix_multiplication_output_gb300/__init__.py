@@ -6,7 +6,7 @@ its ctypes binding plus the seeded input generator.  The library is loaded
 on first use and there is no CPU fallback.
 """
 from .binding import (  # noqa: F401
-    BF16, F16, F32, KERNEL_NAMES, KERNELS, GemmError, error_string, gemm, gemm_debug_config,
-    gemm_device_status, gemm_error_string, gemm_ex, gemm_ex_host, gemm_ex_kernel,
+    BF16, F16, F32, KERNEL_NAMES, KERNELS, GemmError, addmm, error_string, gemm, gemm_debug_config,
+    gemm_device_status, gemm_error_string, gemm_ex, gemm_ex_host, gemm_ex_kernel, gemm_general,
     gemm_select_kernel, header_functions, library_path, load_library, matmul,
 )

@@ -47,6 +47,8 @@ _SIGNATURES = {
     "gemm_ex": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p], _int),
     "gemm_ex_kernel": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _int, _p], _int),
     "gemm_select_kernel": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int], _int),
+    "gemm_general": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, ctypes.c_float, ctypes.c_float,
+                      _int, _int, _int, _int, _p], _int),
     "gemm_ex_host": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, _p, _p, _p], _int),
     "gemm_device_status": ([_p], _int),
     "gemm_debug_config": ([_i64, _int], _int),
@@ -106,6 +108,12 @@ def gemm_ex_kernel(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, kernel, str
                                          kernel, stream)
 
 
+def gemm_general(A, B, C, M, N, K, op_a, op_b, alpha, beta, in_dtype, acc_dtype, out_dtype,
+                 kernel=0, stream=None) -> int:
+    return load_library().gemm_general(A, B, C, M, N, K, op_a, op_b, alpha, beta, in_dtype,
+                                       acc_dtype, out_dtype, kernel, stream)
+
+
 def gemm_select_kernel(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype) -> int:
     return load_library().gemm_select_kernel(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype)
 
@@ -160,6 +168,43 @@ def _stream_handle(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+OPS = {"n": 0, "t": 1}
+
+
+def addmm(A, B, C=None, op_a="n", op_b="n", alpha=1.0, beta=0.0, out_dtype=None,
+          kernel: str | int = "auto", stream=None):
+    """C = alpha * op(A) @ op(B) + beta * C for contiguous CUDA tensors, in place
+    in C when given (C is allocated, and beta must be 0, otherwise).
+
+    op "n" takes an operand as stored, "t" its transpose (A stored K x M, B
+    stored N x K).  Returns C without synchronizing."""
+    torch = _torch()
+    if A.dim() != 2 or B.dim() != 2 or A.dtype != B.dtype:
+        raise ValueError("A and B must be 2-D tensors of one dtype")
+    if not (A.is_cuda and B.is_cuda and A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous CUDA tensors")
+    ta, tb = OPS[op_a], OPS[op_b]
+    M, K = (A.shape[1], A.shape[0]) if ta else (A.shape[0], A.shape[1])
+    K2, N = (B.shape[1], B.shape[0]) if tb else (B.shape[0], B.shape[1])
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        odt = torch.float32 if out_dtype is None else torch_dtype(out_dtype) \
+            if isinstance(out_dtype, (str, int)) else out_dtype
+        C = torch.empty((M, N), dtype=odt, device=A.device)
+    elif tuple(C.shape) != (M, N) or not C.is_contiguous() or not C.is_cuda:
+        raise ValueError("C must be a contiguous (M, N) CUDA tensor")
+    kid = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+    rc = gemm_general(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, ta, tb, float(alpha),
+                      float(beta), dtype_code(A.dtype), F32, dtype_code(C.dtype), kid,
+                      _stream_handle(stream))
+    if rc != OK:
+        raise GemmError(rc, "gemm_general")
+    return C
 
 
 def matmul(A, B, out_dtype=None, kernel: str | int = "auto", out=None, stream=None):

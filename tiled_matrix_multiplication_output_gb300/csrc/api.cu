@@ -80,22 +80,37 @@ int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, 
     return GEMM_OK;
 }
 
+// The operation of one call: C = alpha * op(A) op(B) + beta * C.
+struct Problem {
+    const void* A;
+    const void* B;
+    void* C;
+    int64_t M, N, K;
+    int op_a, op_b;  // 0: as stored; 1: transposed
+    float alpha, beta;
+    int in_dtype, acc_dtype, out_dtype;
+};
+
 // Whether a tensor-core kernel can take these operands: 16-bit inputs, FP32
-// accumulation, 16-byte aligned bases and row pitches (TMA rules).
-bool tc_eligible(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                 int in_dtype, int out_dtype)
+// accumulation, 16-byte aligned bases and row pitches (TMA rules).  The row
+// pitch of A is K elements as stored or M transposed; of B, N as stored or K
+// transposed; of C, N.
+bool tc_eligible(const Problem& q)
 {
-    if (((M + 127) / 128) * ((N + 127) / 128) >= (int64_t(1) << 31))
+    if (((q.M + 127) / 128) * ((q.N + 127) / 128) >= (int64_t(1) << 31))
         return false;  // tile indices are 32-bit
-    if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16)
+    if (q.in_dtype != GEMM_F16 && q.in_dtype != GEMM_BF16)
         return false;
-    if (K <= 0)
+    if (q.K <= 0)
         return false;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C))
+    if (!aligned16(q.A) || !aligned16(q.B) || !aligned16(q.C))
         return false;
-    if ((K * dt_size(in_dtype)) % 16 != 0 || (N * dt_size(in_dtype)) % 16 != 0)
+    const int64_t ib = dt_size(q.in_dtype);
+    const int64_t pitch_a = q.op_a ? q.M : q.K;
+    const int64_t pitch_b = q.op_b ? q.K : q.N;
+    if ((pitch_a * ib) % 16 != 0 || (pitch_b * ib) % 16 != 0)
         return false;
-    if ((N * dt_size(out_dtype)) % 16 != 0)
+    if ((q.N * dt_size(q.out_dtype)) % 16 != 0)
         return false;
     return true;
 }
@@ -103,10 +118,10 @@ bool tc_eligible(const void* A, const void* B, const void* C, int64_t M, int64_t
 // The automatic choice.  Tiny products go to the SIMT kernel (a tensor-core
 // launch has a fixed set-up cost); otherwise the largest tile that still
 // gives every SM work.
-int auto_kernel(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                int in_dtype, int out_dtype, int num_sms)
+int auto_kernel(const Problem& q, int num_sms)
 {
-    if (!tc_eligible(A, B, C, M, N, K, in_dtype, out_dtype))
+    const int64_t M = q.M, N = q.N, K = q.K;
+    if (!tc_eligible(q))
         return GEMM_KERNEL_SIMT;
     const double flops = 2.0 * double(M) * double(N) * double(K);
     if (flops < 2.0 * 64 * 64 * 64)
@@ -120,34 +135,47 @@ int auto_kernel(const void* A, const void* B, const void* C, int64_t M, int64_t 
     return GEMM_KERNEL_TC_128x128;
 }
 
-int run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int in_dtype,
-        int acc_dtype, int out_dtype, int kernel, cudaStream_t stream)
+int validate_problem(const Problem& q)
 {
-    int rc = validate(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype);
+    int rc = validate(q.A, q.B, q.C, q.M, q.N, q.K, q.in_dtype, q.acc_dtype, q.out_dtype);
+    if (rc != GEMM_OK)
+        return rc;
+    if ((q.op_a != GEMM_OP_N && q.op_a != GEMM_OP_T) || (q.op_b != GEMM_OP_N && q.op_b != GEMM_OP_T))
+        return GEMM_ERR_INVALID_VALUE;
+    return GEMM_OK;
+}
+
+int run(const Problem& q, int kernel, cudaStream_t stream)
+{
+    int rc = validate_problem(q);
     if (rc != GEMM_OK)
         return rc;
     if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_TC_256x256)
         return GEMM_ERR_INVALID_VALUE;
-    if (M == 0 || N == 0)
+    if (q.M == 0 || q.N == 0)
         return GEMM_OK;
     DeviceInfo d;
     if (device_info(&d) != cudaSuccess)
         return GEMM_ERR_CUDA;
     if (kernel == GEMM_KERNEL_AUTO)
-        kernel = auto_kernel(A, B, C, M, N, K, in_dtype, out_dtype, d.num_sms);
+        kernel = auto_kernel(q, d.num_sms);
     if (kernel >= GEMM_KERNEL_TC_128x128) {
-        if (!tc_eligible(A, B, C, M, N, K, in_dtype, out_dtype))
+        if (!tc_eligible(q))
             return GEMM_ERR_UNSUPPORTED;
         TcLaunch l{};
         l.variant = kernel;
-        l.in_dtype = in_dtype;
-        l.out_dtype = out_dtype;
-        l.A = A;
-        l.B = B;
-        l.C = C;
-        l.M = static_cast<int>(M);
-        l.N = static_cast<int>(N);
-        l.K = static_cast<int>(K);
+        l.op_a = q.op_a;
+        l.op_b = q.op_b;
+        l.alpha = q.alpha;
+        l.beta = q.beta;
+        l.in_dtype = q.in_dtype;
+        l.out_dtype = q.out_dtype;
+        l.A = q.A;
+        l.B = q.B;
+        l.C = q.C;
+        l.M = static_cast<int>(q.M);
+        l.N = static_cast<int>(q.N);
+        l.K = static_cast<int>(q.K);
         l.num_sms = d.num_sms;
         l.status = d.status;
         l.wait_budget = g_wait_budget.load();
@@ -157,10 +185,30 @@ int run(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, 
             return GEMM_ERR_UNSUPPORTED;
         return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
-    cudaError_t err = simt_gemm_launch(kernel == GEMM_KERNEL_SIMT_TPB3, in_dtype, out_dtype, A, B,
-                                       C, static_cast<int>(M), static_cast<int>(N),
-                                       static_cast<int>(K), d.num_sms, stream);
+    SimtLaunch l{};
+    l.tpb3 = (kernel == GEMM_KERNEL_SIMT_TPB3);
+    l.in_dtype = q.in_dtype;
+    l.out_dtype = q.out_dtype;
+    l.op_a = q.op_a;
+    l.op_b = q.op_b;
+    l.alpha = q.alpha;
+    l.beta = q.beta;
+    l.A = q.A;
+    l.B = q.B;
+    l.C = q.C;
+    l.M = static_cast<int>(q.M);
+    l.N = static_cast<int>(q.N);
+    l.K = static_cast<int>(q.K);
+    l.num_sms = d.num_sms;
+    cudaError_t err = simt_gemm_launch(l, stream);
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+Problem plain(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int in_dtype,
+              int acc_dtype, int out_dtype)
+{
+    return Problem{A, B, C, M, N, K, GEMM_OP_N, GEMM_OP_N, 1.0f, 0.0f, in_dtype, acc_dtype,
+                   out_dtype};
 }
 
 }  // namespace
@@ -171,7 +219,7 @@ using namespace tmmo;
 extern "C" int gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                     gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, void* stream)
 {
-    return run(A, B, C, M, N, K, in_dtype, acc_dtype, acc_dtype, GEMM_KERNEL_AUTO,
+    return run(plain(A, B, C, M, N, K, in_dtype, acc_dtype, acc_dtype), GEMM_KERNEL_AUTO,
                static_cast<cudaStream_t>(stream));
 }
 
@@ -179,7 +227,7 @@ extern "C" int gemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t
                        gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
                        void* stream)
 {
-    return run(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, GEMM_KERNEL_AUTO,
+    return run(plain(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype), GEMM_KERNEL_AUTO,
                static_cast<cudaStream_t>(stream));
 }
 
@@ -187,21 +235,31 @@ extern "C" int gemm_ex_kernel(const void* A, const void* B, void* C, int64_t M, 
                               int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
                               gemm_dtype_t out_dtype, gemm_kernel_t kernel, void* stream)
 {
-    return run(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, kernel,
+    return run(plain(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype), kernel,
                static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gemm_general(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                            int64_t K, gemm_op_t op_a, gemm_op_t op_b, float alpha, float beta,
+                            gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
+                            gemm_kernel_t kernel, void* stream)
+{
+    const Problem q{A, B, C, M, N, K, op_a, op_b, alpha, beta, in_dtype, acc_dtype, out_dtype};
+    return run(q, kernel, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gemm_select_kernel(const void* A, const void* B, const void* C, int64_t M,
                                   int64_t N, int64_t K, gemm_dtype_t in_dtype,
                                   gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype)
 {
-    int rc = validate(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype);
+    const Problem q = plain(A, B, const_cast<void*>(C), M, N, K, in_dtype, acc_dtype, out_dtype);
+    int rc = validate_problem(q);
     if (rc != GEMM_OK)
         return -rc;
     DeviceInfo d;
     if (device_info(&d) != cudaSuccess)
         return -GEMM_ERR_CUDA;
-    return auto_kernel(A, B, C, M, N, K, in_dtype, out_dtype, d.num_sms);
+    return auto_kernel(q, d.num_sms);
 }
 
 extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
@@ -226,7 +284,7 @@ extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host
                 cudaSuccess)
             return GEMM_ERR_CUDA;
     }
-    rc = run(dA, dB, dC, M, N, K, in_dtype, acc_dtype, out_dtype, GEMM_KERNEL_AUTO, s);
+    rc = run(plain(dA, dB, dC, M, N, K, in_dtype, acc_dtype, out_dtype), GEMM_KERNEL_AUTO, s);
     if (rc != GEMM_OK)
         return rc;
     if (cudaMemcpyAsync(C_host, dC, size_t(M) * size_t(N) * out_b, cudaMemcpyDeviceToHost, s) !=

@@ -13,11 +13,24 @@ enum { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 // Tensor-core kernel variants; they match the gemm_kernel_t values.
 enum { TC_128x128 = 3, TC_128x256 = 4, TC_256x256 = 5 };
 
-cudaError_t simt_gemm_launch(bool tpb3, int in_dtype, int out_dtype, const void* A, const void* B,
-                             void* C, int M, int N, int K, int num_sms, cudaStream_t stream);
+struct SimtLaunch {
+    bool tpb3;          // the 3 x 3 one-thread-per-output instance
+    int in_dtype, out_dtype;
+    int op_a, op_b;     // 0: as stored; 1: transposed
+    float alpha, beta;
+    const void* A;
+    const void* B;
+    void* C;
+    int M, N, K;
+    int num_sms;
+};
+
+cudaError_t simt_gemm_launch(const SimtLaunch& l, cudaStream_t stream);
 
 struct TcLaunch {
     int variant;        // TC_128x128, TC_128x256 or TC_256x256
+    int op_a, op_b;     // 0: as stored; 1: transposed (A stored K x M, B stored N x K)
+    float alpha, beta;  // C = alpha * op(A) op(B) + beta * C
     int in_dtype;       // DT_F16 or DT_BF16
     int out_dtype;      // DT_F32, DT_F16 or DT_BF16
     const void* A;
@@ -34,6 +47,13 @@ struct TcLaunch {
 // cudaErrorNotSupported when the driver entry point for tensor maps is
 // unavailable.
 cudaError_t tc_gemm_launch(const TcLaunch& l, cudaStream_t stream);
+cudaError_t tc_launch_nn(const TcLaunch& l, cudaStream_t stream);
+cudaError_t tc_launch_tn(const TcLaunch& l, cudaStream_t stream);
+cudaError_t tc_launch_nt(const TcLaunch& l, cudaStream_t stream);
+cudaError_t tc_launch_tt(const TcLaunch& l, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled from the driver (as void*), or null if unavailable.
+void* tensor_map_encoder();
 
 // Output tile of a tensor-core variant (rows x columns).
 void tc_tile_shape(int variant, int* tile_m, int* tile_n);

@@ -21,7 +21,11 @@
 //    share the kernel; the FP32 result is rounded to the output type with
 //    round-to-nearest-even;
 //  * the grid is 1-D and each block strides over output tiles, so any M, N
-//    fit the launch limits.
+//    fit the launch limits;
+//  * transposed operands (A stored K x M, B stored N x K) are read through
+//    strides, with the staging loop walking the contiguous dimension so
+//    global reads stay coalesced; the store computes alpha * acc + beta * C
+//    (C read only when beta != 0).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -42,10 +46,14 @@ __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__half* p, float v) { *p = __float2half_rn(v); }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+__device__ __forceinline__ float load_out(const float* p) { return *p; }
+__device__ __forceinline__ float load_out(const __half* p) { return __half2float(*p); }
+__device__ __forceinline__ float load_out(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
 template <int BM, int BN, int BK, int TM, int TN, typename InT, typename OutT>
 __global__ void __launch_bounds__((BM / TM) * (BN / TN))
-    simt_gemm_kernel(const InT* __restrict__ A, const InT* __restrict__ B, OutT* __restrict__ C,
-                     int M, int N, int K)
+    simt_gemm_kernel(const InT* __restrict__ A, const InT* __restrict__ B, OutT* C, int M, int N,
+                     int K, int op_a, int op_b, float alpha, float beta)
 {
     constexpr int TX = BN / TN;  // threads along N
     constexpr int TY = BM / TM;  // threads along M
@@ -72,19 +80,26 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
                 acc[i][j] = 0.0f;
 
         for (int k0 = 0; k0 < K; k0 += BK) {
-            // Stage the A tile (BM x BK): consecutive threads read
-            // consecutive k of one row (coalesced), stored K-major.
+            // Stage the A tile (BM x BK), stored K-major; consecutive
+            // threads walk the dimension that is contiguous in memory (k for
+            // A as stored, m for A transposed), so global reads coalesce.
             for (int e = tid; e < BM * BK; e += NT) {
-                const int i = e / BK, k = e % BK;
+                const int i = op_a ? e % BM : e / BK;
+                const int k = op_a ? e / BM : e % BK;
                 const int gm = m0 + i, gk = k0 + k;
-                As[k][i] = (gm < M && gk < K) ? to_f32(A[static_cast<long long>(gm) * K + gk]) : 0.0f;
+                const long long off = op_a ? static_cast<long long>(gk) * M + gm
+                                           : static_cast<long long>(gm) * K + gk;
+                As[k][i] = (gm < M && gk < K) ? to_f32(A[off]) : 0.0f;
             }
-            // Stage the B tile (BK x BN): consecutive threads read
-            // consecutive columns of one row (coalesced).
+            // Stage the B tile (BK x BN): n contiguous for B as stored, k for
+            // B transposed.
             for (int e = tid; e < BK * BN; e += NT) {
-                const int k = e / BN, j = e % BN;
+                const int k = op_b ? e % BK : e / BN;
+                const int j = op_b ? e / BK : e % BN;
                 const int gk = k0 + k, gn = n0 + j;
-                Bs[k][j] = (gk < K && gn < N) ? to_f32(B[static_cast<long long>(gk) * N + gn]) : 0.0f;
+                const long long off = op_b ? static_cast<long long>(gn) * K + gk
+                                           : static_cast<long long>(gk) * N + gn;
+                Bs[k][j] = (gk < K && gn < N) ? to_f32(B[off]) : 0.0f;
             }
             __syncthreads();
 #pragma unroll
@@ -113,64 +128,64 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
 #pragma unroll
             for (int j = 0; j < TN; ++j) {
                 const int gn = n0 + tx + j * TX;
-                if (gn < N)
-                    store_out(C + static_cast<long long>(gm) * N + gn, acc[i][j]);
+                if (gn < N) {
+                    OutT* dst = C + static_cast<long long>(gm) * N + gn;
+                    const float v = (beta != 0.0f) ? fmaf(beta, load_out(dst), alpha * acc[i][j])
+                                                   : alpha * acc[i][j];
+                    store_out(dst, v);
+                }
             }
         }
     }
 }
 
 template <int BM, int BN, int BK, int TM, int TN, typename InT, typename OutT>
-cudaError_t launch_simt(const void* A, const void* B, void* C, int M, int N, int K, int num_sms,
-                        cudaStream_t stream)
+cudaError_t launch_simt(const SimtLaunch& l, cudaStream_t stream)
 {
     constexpr int NT = (BM / TM) * (BN / TN);
-    const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const long long tiles = static_cast<long long>((l.M + BM - 1) / BM) * ((l.N + BN - 1) / BN);
     // Enough blocks for several resident per SM; each strides over tiles.
-    const long long cap = static_cast<long long>(std::max(num_sms, 1)) * 16;
+    const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 16;
     const int grid = static_cast<int>(std::max<long long>(1, std::min(tiles, cap)));
     simt_gemm_kernel<BM, BN, BK, TM, TN, InT, OutT><<<grid, NT, 0, stream>>>(
-        static_cast<const InT*>(A), static_cast<const InT*>(B), static_cast<OutT*>(C), M, N, K);
+        static_cast<const InT*>(l.A), static_cast<const InT*>(l.B), static_cast<OutT*>(l.C), l.M,
+        l.N, l.K, l.op_a, l.op_b, l.alpha, l.beta);
     return cudaGetLastError();
 }
 
 template <int BM, int BN, int BK, int TM, int TN, typename InT>
-cudaError_t dispatch_out(int out_dtype, const void* A, const void* B, void* C, int M, int N,
-                         int K, int num_sms, cudaStream_t s)
+cudaError_t dispatch_out(const SimtLaunch& l, cudaStream_t s)
 {
-    switch (out_dtype) {
+    switch (l.out_dtype) {
     case DT_F32:
-        return launch_simt<BM, BN, BK, TM, TN, InT, float>(A, B, C, M, N, K, num_sms, s);
+        return launch_simt<BM, BN, BK, TM, TN, InT, float>(l, s);
     case DT_F16:
-        return launch_simt<BM, BN, BK, TM, TN, InT, __half>(A, B, C, M, N, K, num_sms, s);
+        return launch_simt<BM, BN, BK, TM, TN, InT, __half>(l, s);
     default:
-        return launch_simt<BM, BN, BK, TM, TN, InT, __nv_bfloat16>(A, B, C, M, N, K, num_sms, s);
+        return launch_simt<BM, BN, BK, TM, TN, InT, __nv_bfloat16>(l, s);
     }
 }
 
 template <int BM, int BN, int BK, int TM, int TN>
-cudaError_t dispatch_in(int in_dtype, int out_dtype, const void* A, const void* B, void* C, int M,
-                        int N, int K, int num_sms, cudaStream_t s)
+cudaError_t dispatch_in(const SimtLaunch& l, cudaStream_t s)
 {
-    switch (in_dtype) {
+    switch (l.in_dtype) {
     case DT_F32:
-        return dispatch_out<BM, BN, BK, TM, TN, float>(out_dtype, A, B, C, M, N, K, num_sms, s);
+        return dispatch_out<BM, BN, BK, TM, TN, float>(l, s);
     case DT_F16:
-        return dispatch_out<BM, BN, BK, TM, TN, __half>(out_dtype, A, B, C, M, N, K, num_sms, s);
+        return dispatch_out<BM, BN, BK, TM, TN, __half>(l, s);
     default:
-        return dispatch_out<BM, BN, BK, TM, TN, __nv_bfloat16>(out_dtype, A, B, C, M, N, K,
-                                                                num_sms, s);
+        return dispatch_out<BM, BN, BK, TM, TN, __nv_bfloat16>(l, s);
     }
 }
 
 }  // namespace
 
-cudaError_t simt_gemm_launch(bool tpb3, int in_dtype, int out_dtype, const void* A, const void* B,
-                             void* C, int M, int N, int K, int num_sms, cudaStream_t stream)
+cudaError_t simt_gemm_launch(const SimtLaunch& l, cudaStream_t stream)
 {
-    if (tpb3)
-        return dispatch_in<3, 3, 3, 1, 1>(in_dtype, out_dtype, A, B, C, M, N, K, num_sms, stream);
-    return dispatch_in<64, 64, 16, 4, 4>(in_dtype, out_dtype, A, B, C, M, N, K, num_sms, stream);
+    if (l.tpb3)
+        return dispatch_in<3, 3, 3, 1, 1>(l, stream);
+    return dispatch_in<64, 64, 16, 4, 4>(l, stream);
 }
 
 }  // namespace tmmo

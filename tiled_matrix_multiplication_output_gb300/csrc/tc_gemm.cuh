@@ -26,6 +26,15 @@
 //     (which add exactly nothing), so partial edge tiles in M, N and K are
 //     exact ("Edge tiles still matter").
 //
+// Operands may also be given transposed ("Tiled Matrix Multiplication",
+// "When would transposed loading be useful?"): op(A) = A^T is A stored K x M
+// (M contiguous, an MN-major tcgen05 operand) and op(B) = B^T is B stored
+// N x K (K contiguous, a K-major operand).  The template flags A_MN / B_MN
+// select the box shapes and shared-memory descriptors; nothing is transposed
+// in memory.  The epilogue can also compute alpha * acc + beta * C_in, the
+// accumulate-into-C form of the helion kernel's torch.addmm ("Writing a
+// matmul GPU kernel").
+//
 // CG = 2 runs the same protocol on a CTA pair (cta_group::2): each CTA loads
 // its own 128 rows of A and half of the B columns, the leader CTA issues
 // M = 256 MMAs that read both CTAs' shared memory, and each CTA's TMEM holds
@@ -76,14 +85,15 @@ struct TcLayout {
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: F32 accumulator (bits
-// 4-5 = 1), A/B type F16 (0) or BF16 (1) in bits 7-9 / 10-12, A K-major
-// (bit 15 = 0), B N-major (bit 16 = 1), N >> 3 in bits 17-22 and M >> 4 in
-// bits 24-28.
-__host__ __device__ constexpr uint32_t tc_idesc(bool bf16, int m, int n)
+// 4-5 = 1), A/B type F16 (0) or BF16 (1) in bits 7-9 / 10-12, A major-ness
+// in bit 15 and B major-ness in bit 16 (0 = K-major, 1 = MN-major), N >> 3 in
+// bits 17-22 and M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t tc_idesc(bool bf16, int m, int n, bool a_mn = false,
+                                                bool b_mn = true)
 {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | (0u << 15) |
-           (1u << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
-           (static_cast<uint32_t>(m >> 4) << 24);
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // Grouped raster order: tiles are taken `group_m` tile-rows at a time and,
@@ -173,15 +183,55 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // from TMEM, convert, and write it to a swizzled staging buffer: 16-byte
 // chunk c of row r goes to chunk position c ^ (r % 8), the layout a
 // SWIZZLE_128B TMA store expects, and conflict-free for 8 rows at a time.
+__device__ __forceinline__ float out_to_f32(float v) { return v; }
+__device__ __forceinline__ float out_to_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float out_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// v[i] <- alpha * v[i] + beta * C_in[grow, gcol + i] for the `n` values of one
+// 16-byte chunk of this thread's row (n = 4 FP32 or 8 16-bit values).  The
+// chunk is read only if it lies inside C; N * sizeof(OutT) is a multiple of
+// 16, so chunks never straddle the right edge.
+template <typename OutT, int n>
+__device__ __forceinline__ void tc_axpby_chunk(float* v, const TcParams& p, int grow, int gcol)
+{
+    if (p.beta != 0.0f && grow < p.M && gcol < p.N) {
+        const OutT* src = static_cast<const OutT*>(p.C) + static_cast<long long>(grow) * p.N + gcol;
+        const uint4 raw = *reinterpret_cast<const uint4*>(src);
+        const OutT* e = reinterpret_cast<const OutT*>(&raw);
+#pragma unroll
+        for (int i = 0; i < n; ++i)
+            v[i] = fmaf(p.beta, out_to_f32(e[i]), p.alpha * v[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < n; ++i)
+            v[i] = p.alpha * v[i];
+    }
+}
+
 template <typename OutT>
-__device__ __forceinline__ void tc_strip_to_smem(uint32_t taddr, uint32_t staging, uint32_t row)
+__device__ __forceinline__ void tc_strip_to_smem(uint32_t taddr, uint32_t staging, uint32_t row,
+                                                 const TcParams& p, int grow, int gcol0)
 {
     const uint32_t row_base = staging + row * 128;
     const uint32_t sw = row & 7;
+    const bool scale = (p.alpha != 1.0f) || (p.beta != 0.0f);
     if constexpr (sizeof(OutT) == 4) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr, v);
         tmem_wait_ld();
+        if (scale) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float f[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    f[i] = __uint_as_float(v[4 * c + i]);
+                tc_axpby_chunk<OutT, 4>(f, p, grow, gcol0 + 4 * c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    v[4 * c + i] = __float_as_uint(f[i]);
+            }
+        }
 #pragma unroll
         for (int c = 0; c < 8; ++c)
             st_shared_v4(row_base + ((c ^ sw) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
@@ -196,16 +246,19 @@ __device__ __forceinline__ void tc_strip_to_smem(uint32_t taddr, uint32_t stagin
         for (int c = 0; c < 8; ++c) {
             const uint32_t* src = (c < 4) ? lo : hi;
             const int b = (c & 3) * 8;
-            uint32_t w0 = pack2(__uint_as_float(src[b + 0]), __uint_as_float(src[b + 1]), tag);
-            uint32_t w1 = pack2(__uint_as_float(src[b + 2]), __uint_as_float(src[b + 3]), tag);
-            uint32_t w2 = pack2(__uint_as_float(src[b + 4]), __uint_as_float(src[b + 5]), tag);
-            uint32_t w3 = pack2(__uint_as_float(src[b + 6]), __uint_as_float(src[b + 7]), tag);
-            st_shared_v4(row_base + ((c ^ sw) << 4), w0, w1, w2, w3);
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                f[i] = __uint_as_float(src[b + i]);
+            if (scale)
+                tc_axpby_chunk<OutT, 8>(f, p, grow, gcol0 + 8 * c);
+            st_shared_v4(row_base + ((c ^ sw) << 4), pack2(f[0], f[1], tag), pack2(f[2], f[3], tag),
+                         pack2(f[4], f[5], tag), pack2(f[6], f[7], tag));
         }
     }
 }
 
-template <int CG, int BN, int STAGES, typename OutT>
+template <int CG, int BN, int STAGES, typename OutT, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p)
@@ -291,16 +344,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             mbar_arrive_expect_tx(full_bar(stage), CG * L::STAGE_BYTES);
                         const uint32_t dA = sA + stage * L::A_STAGE;
                         const uint32_t dB = sB + stage * L::B_STAGE;
-                        if constexpr (CG == 2) {
-                            tma_load_2d_pair(dA, &tmA, fb, kb * TC_BK, a_row);
-#pragma unroll
-                            for (int j = 0; j < L::B_BOXES; ++j)
-                                tma_load_2d_pair(dB + j * 8192, &tmB, fb, b_col + 64 * j, kb * TC_BK);
+                        auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
+                            if constexpr (CG == 2)
+                                tma_load_2d_pair(dst, map, fb, x, y);
+                            else
+                                tma_load_2d(dst, map, fb, x, y);
+                        };
+                        // A: K-major, one 128-row x 64-K box; or MN-major
+                        // (A stored K x M), two 64-K x 64-M boxes.
+                        if constexpr (A_MN) {
+                            load(dA, &tmA, a_row, kb * TC_BK);
+                            load(dA + 8192, &tmA, a_row + 64, kb * TC_BK);
                         } else {
-                            tma_load_2d(dA, &tmA, fb, kb * TC_BK, a_row);
+                            load(dA, &tmA, kb * TC_BK, a_row);
+                        }
+                        // B: MN-major (B stored K x N), 64-K x 64-N boxes; or
+                        // K-major (B stored N x K), one B_COLS-row x 64-K box.
+                        if constexpr (B_MN) {
 #pragma unroll
                             for (int j = 0; j < L::B_BOXES; ++j)
-                                tma_load_2d(dB + j * 8192, &tmB, fb, b_col + 64 * j, kb * TC_BK);
+                                load(dB + j * 8192, &tmB, b_col + 64 * j, kb * TC_BK);
+                        } else {
+                            load(dB, &tmB, kb * TC_BK, b_col);
                         }
                         ++issued[stage];
                     }
@@ -352,12 +417,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t b0 = sB + stage * L::B_STAGE;
 #pragma unroll
                     for (int k = 0; k < TC_BK / TC_UMMA_K; ++k) {
-                        // A: K-major rows of 128 bytes, 8-row groups 1024 bytes
-                        // apart; a K step of 16 moves 32 bytes along the row.
-                        const uint64_t adesc = smem_desc_sw128(a0 + k * 32, 16, 1024);
-                        // B: N-major, 64-column atoms 8 KiB apart (LBO), 8-row
-                        // K groups 1024 bytes apart (SBO); 16 K rows = 2 KiB.
-                        const uint64_t bdesc = smem_desc_sw128(b0 + k * 2048, 8192, 1024);
+                        // K-major operand: rows of 128 bytes, 8-row groups 1024
+                        // bytes apart (SBO); a K step of 16 moves 32 bytes
+                        // along the row.  MN-major operand: 64-element atoms
+                        // 8 KiB apart (LBO), 8-row K groups 1024 bytes apart
+                        // (SBO); a K step of 16 rows moves 2 KiB.
+                        const uint64_t adesc = A_MN ? smem_desc_sw128(a0 + k * 2048, 8192, 1024)
+                                                    : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                        const uint64_t bdesc = B_MN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
+                                                    : smem_desc_sw128(b0 + k * 32, 16, 1024);
                         tc_mma_f16<CG>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
                     }
                     if constexpr (CG == 2)
@@ -418,7 +486,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (lane == 0)
                     bulk_wait_group_read<1>();
                 __syncwarp();
-                tc_strip_to_smem<OutT>(t_row + s * STRIP, stg, lane);
+                tc_strip_to_smem<OutT>(t_row + s * STRIP, stg, lane, p,
+                                       row0 + static_cast<int>(lane), col0);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

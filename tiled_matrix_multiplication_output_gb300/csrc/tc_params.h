@@ -17,6 +17,8 @@ struct TcParams {
     int* status;                       // device status word (never null)
     long long wait_budget;             // clock cycles a single wait may take
     int fault_skip_kblock;             // test hook: K step whose loads are skipped; -1 = none
+    const void* C;                     // the output, read as C_in when beta != 0
+    float alpha, beta;                 // C = alpha * acc + beta * C_in
 };
 
 }  // namespace tmmo
