@@ -31,6 +31,7 @@
 #ifndef TILED_GEMM_H
 #define TILED_GEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -140,6 +141,39 @@ int gemm_general(const void* A, const void* B, void* C, int64_t M, int64_t N, in
                  gemm_op_t op_a, gemm_op_t op_b, float alpha, float beta, gemm_dtype_t in_dtype,
                  gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype, gemm_kernel_t kernel,
                  void* stream);
+
+/*
+ * gemm_splitk_workspace_size -- bytes of FP32 workspace gemm_splitk needs:
+ * used_splits * M * N * 4, where used_splits <= splits is the number of
+ * equal ranges of 64-wide K steps K is divided into (no range is empty).
+ * Returns 0 for non-positive sizes or splits < 1.
+ */
+size_t gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int splits);
+
+/*
+ * gemm_splitk -- C = A @ B (as gemm_ex) with the K reduction split across
+ * SMs, for products with few output tiles and a long K.
+ *
+ * "Reading a matrix multiply through its tiles" ("Keep one output tile
+ * resident") accumulates each output tile over all of K before writing it
+ * once; here each tile's K steps are divided into `splits` ranges that run
+ * as separate units of work, each range's FP32 partial tile is written to
+ * `workspace` (split-major, [split][M][N], caller-owned device memory of at
+ * least gemm_splitk_workspace_size bytes, 16-byte aligned), and a second
+ * kernel on the same stream adds the partials in split order (a fixed
+ * order: the result is identical run to run) and writes C in out_dtype with
+ * round-to-nearest-even.  The workspace contents are scratch: they need no
+ * initial value and are overwritten.  Two calls that share a workspace must
+ * not overlap in time.
+ *
+ * Operands the tensor-core kernels cannot take (see gemm_ex_kernel) are
+ * computed by gemm_ex's automatic choice instead; the workspace is then not
+ * used.  Returns as gemm_ex, plus GEMM_ERR_INVALID_VALUE for splits < 1 or a
+ * missing, misaligned or too small workspace.
+ */
+int gemm_splitk(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                int splits, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                gemm_dtype_t out_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * gemm_select_kernel -- the kernel gemm_ex would launch for these arguments

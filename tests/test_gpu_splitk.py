@@ -1,0 +1,76 @@
+"""Split-K (gemm_splitk) on the GPU: FP32 partials per K range in a caller
+workspace, summed in split order.  Exact on integer inputs, within the bound
+on random inputs, identical run to run, and argument checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_matrix_multiplication_output_gb300 as tg
+from tests.helpers import expect_exact, tolerance_check
+from tiled_matrix_multiplication_output_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    tg.gemm_debug_config(0, -1)
+
+
+def _splitk(A, B, splits, out_dtype=torch.float32):
+    C = tg.matmul_splitk(A.cuda(), B.cuda(), splits, out_dtype=out_dtype)
+    assert tg.gemm_device_status(torch.cuda.current_stream().cuda_stream) == 0
+    return C.cpu()
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 16, 1000])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
+def test_splitk_exact_integers(splits, out_dtype):
+    """The edge-tile workload's shape (96 x 200 x 1000): partial tiles in M, N
+    and K; integer inputs, so every split count gives the exact product."""
+    A, B = inputs.draw(96, 200, 1000, "bf16", "int", seed=70)
+    expect_exact(_splitk(A, B, splits, out_dtype), A, B)
+
+
+def test_splitk_edge_workload_within_bound():
+    w = inputs.WORKLOADS["edge_96x200x1000_bf16"]
+    A, B = inputs.make(w)
+    ref, Cabs = oracle.gemm(A, B)
+    for splits in (2, 4, 8, 16):
+        tolerance_check(_splitk(A, B, splits), ref, Cabs, with_output_rounding=False)
+
+
+def test_splitk_long_k_many_splits():
+    A, B = inputs.draw(256, 264, 16392, "f16", "uniform", seed=71)
+    ref, Cabs = oracle.gemm(A, B)
+    C = _splitk(A, B, 48)
+    tolerance_check(C, ref, Cabs, with_output_rounding=False)
+    C2 = _splitk(A, B, 48)
+    assert torch.equal(C, C2)
+
+
+def test_workspace_size_and_checks():
+    assert tg.gemm_splitk_workspace_size(96, 200, 1000, 4) == 4 * 96 * 200 * 4
+    # 16 K steps into 5 ranges: 4 steps per range, 4 ranges used
+    assert tg.gemm_splitk_workspace_size(96, 200, 1000, 5) == 4 * 96 * 200 * 4
+    assert tg.gemm_splitk_workspace_size(96, 200, 1000, 1000) == 16 * 96 * 200 * 4
+    assert tg.gemm_splitk_workspace_size(0, 200, 1000, 4) == 0
+    A = torch.zeros(96, 1000, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(1000, 200, dtype=torch.bfloat16, device="cuda")
+    C = torch.empty(96, 200, device="cuda")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    rc = tg.gemm_splitk(A.data_ptr(), B.data_ptr(), C.data_ptr(), 96, 200, 1000, 4, tg.BF16,
+                        tg.F32, tg.F32, ws.data_ptr(), 1024, None)
+    assert rc == tg.binding.ERR_INVALID_VALUE       # workspace too small
+    rc = tg.gemm_splitk(A.data_ptr(), B.data_ptr(), C.data_ptr(), 96, 200, 1000, 0, tg.BF16,
+                        tg.F32, tg.F32, ws.data_ptr(), 1024, None)
+    assert rc == tg.binding.ERR_INVALID_VALUE       # splits < 1
+
+
+def test_splitk_unaligned_falls_back_exactly():
+    A, B = inputs.draw(50, 37, 333, "f16", "int", seed=72)   # no TMA-legal pitches
+    C = tg.matmul_splitk(A.cuda(), B.cuda(), 4)
+    expect_exact(C.cpu(), A, B)

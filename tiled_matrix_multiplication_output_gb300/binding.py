@@ -50,6 +50,9 @@ _SIGNATURES = {
     "gemm_general": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, ctypes.c_float, ctypes.c_float,
                       _int, _int, _int, _int, _p], _int),
     "gemm_ex_host": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, _p, _p, _p], _int),
+    "gemm_splitk_workspace_size": ([_i64, _i64, _i64, _int], ctypes.c_size_t),
+    "gemm_splitk": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _int, _p, ctypes.c_size_t,
+                     _p], _int),
     "gemm_device_status": ([_p], _int),
     "gemm_debug_config": ([_i64, _int], _int),
     "gemm_error_string": ([_int], ctypes.c_char_p),
@@ -122,6 +125,38 @@ def gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype
                  stream=None) -> int:
     return load_library().gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype,
                                        out_dtype, dA, dB, dC, stream)
+
+
+def gemm_splitk_workspace_size(M, N, K, splits) -> int:
+    return load_library().gemm_splitk_workspace_size(M, N, K, splits)
+
+
+def gemm_splitk(A, B, C, M, N, K, splits, in_dtype, acc_dtype, out_dtype, workspace,
+                workspace_bytes, stream=None) -> int:
+    return load_library().gemm_splitk(A, B, C, M, N, K, splits, in_dtype, acc_dtype, out_dtype,
+                                      workspace, workspace_bytes, stream)
+
+
+def matmul_splitk(A, B, splits: int, out_dtype=None, workspace=None, stream=None):
+    """C = A @ B through gemm_splitk for contiguous CUDA tensors.  The FP32
+    workspace is allocated by PyTorch unless given (a CUDA tensor of at
+    least gemm_splitk_workspace_size bytes)."""
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[1]
+    odt = torch.float32 if out_dtype is None else (
+        torch_dtype(out_dtype) if isinstance(out_dtype, (str, int)) else out_dtype)
+    C = torch.empty((M, N), dtype=odt, device=A.device)
+    need = gemm_splitk_workspace_size(M, N, K, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=A.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = gemm_splitk(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(splits),
+                     dtype_code(A.dtype), F32, dtype_code(odt), workspace.data_ptr(), nbytes,
+                     _stream_handle(stream))
+    if rc != OK:
+        raise GemmError(rc, "gemm_splitk")
+    return C
 
 
 def gemm_device_status(stream=None) -> int:

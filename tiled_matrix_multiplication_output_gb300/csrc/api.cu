@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstddef>
 #include <cstdint>
 #include <mutex>
 
@@ -260,6 +261,62 @@ extern "C" int gemm_select_kernel(const void* A, const void* B, const void* C, i
     if (device_info(&d) != cudaSuccess)
         return -GEMM_ERR_CUDA;
     return auto_kernel(q, d.num_sms);
+}
+
+extern "C" size_t gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int splits)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || splits < 1)
+        return 0;
+    const int used = splitk_used_splits(K, splits);
+    return static_cast<size_t>(used) * static_cast<size_t>(M) * static_cast<size_t>(N) * 4u;
+}
+
+extern "C" int gemm_splitk(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                           int splits, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                           gemm_dtype_t out_dtype, void* workspace, size_t workspace_bytes,
+                           void* stream)
+{
+    const Problem q = plain(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype);
+    int rc = validate_problem(q);
+    if (rc != GEMM_OK)
+        return rc;
+    if (splits < 1)
+        return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!tc_eligible(q))
+        return run(q, GEMM_KERNEL_AUTO, s);  // no workspace needed or used
+    const size_t need = gemm_splitk_workspace_size(M, N, K, splits);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+        return GEMM_ERR_INVALID_VALUE;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    TcLaunch l{};
+    l.variant = TC_128x128;
+    l.op_a = GEMM_OP_N;
+    l.op_b = GEMM_OP_N;
+    l.alpha = 1.0f;
+    l.beta = 0.0f;
+    l.in_dtype = in_dtype;
+    l.out_dtype = out_dtype;
+    l.A = A;
+    l.B = B;
+    l.C = C;
+    l.M = static_cast<int>(M);
+    l.N = static_cast<int>(N);
+    l.K = static_cast<int>(K);
+    l.num_sms = d.num_sms;
+    l.status = d.status;
+    l.wait_budget = g_wait_budget.load();
+    l.fault_skip_kblock = g_fault_skip_kblock.load();
+    l.k_splits = splits;
+    l.workspace = static_cast<float*>(workspace);
+    cudaError_t err = tc_splitk_launch(l, nullptr, s);
+    if (err == cudaErrorNotSupported)
+        return GEMM_ERR_UNSUPPORTED;
+    return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M,

@@ -41,6 +41,8 @@ struct TcLaunch {
     int* status;        // device status word
     long long wait_budget;
     int fault_skip_kblock;
+    int k_splits;       // split-K only: requested K ranges per tile
+    float* workspace;   // split-K only: [k_splits][M][N] FP32 partials
 };
 
 // Encodes the tensor maps and launches; returns cudaSuccess, a CUDA error, or
@@ -51,6 +53,16 @@ cudaError_t tc_launch_nn(const TcLaunch& l, cudaStream_t stream);
 cudaError_t tc_launch_tn(const TcLaunch& l, cudaStream_t stream);
 cudaError_t tc_launch_nt(const TcLaunch& l, cudaStream_t stream);
 cudaError_t tc_launch_tt(const TcLaunch& l, cudaStream_t stream);
+
+// Split-K: the tensor-core kernel writes FP32 partial tiles for every range
+// of K steps into l.workspace, then a reduction kernel sums them in split
+// order into C (alpha, beta applied there).  Returns the split count used
+// through *used_splits.
+cudaError_t tc_splitk_launch(const TcLaunch& l, int* used_splits, cudaStream_t stream);
+
+// K ranges split-K actually uses for `requested` ranges of a K extent: every
+// range holds the same whole number of 64-wide K steps and none is empty.
+int splitk_used_splits(int64_t K, int requested);
 
 // cuTensorMapEncodeTiled from the driver (as void*), or null if unavailable.
 void* tensor_map_encoder();

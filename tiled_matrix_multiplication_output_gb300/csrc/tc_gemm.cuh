@@ -35,6 +35,10 @@
 // accumulate-into-C form of the helion kernel's torch.addmm ("Writing a
 // matmul GPU kernel").
 //
+// Split-K (SPLIT = true): a unit of work is an output tile and one range of
+// K steps; its FP32 partial goes to a workspace [split][M][N] through a 3-D
+// TMA store, and a separate kernel sums the partials in split order.
+//
 // CG = 2 runs the same protocol on a CTA pair (cta_group::2): each CTA loads
 // its own 128 rows of A and half of the B columns, the leader CTA issues
 // M = 256 MMAs that read both CTAs' shared memory, and each CTA's TMEM holds
@@ -107,6 +111,26 @@ __device__ __forceinline__ void tc_tile_coords(int t, const TcParams& p, int& mb
     const int r = t - g * per_group;
     mb = first_m + r % gm;
     nb = r / gm;
+}
+
+// One unit of work: an output tile and the range of K steps it accumulates.
+// Without split-K (k_splits = 1) a unit is a whole tile; with split-K, unit
+// t covers tile t % num_tiles over K split t / num_tiles.
+struct TcWork {
+    int mb, nb;
+    int kb_begin, kb_end;
+    int split;
+};
+
+__device__ __forceinline__ TcWork tc_work(int t, const TcParams& p)
+{
+    TcWork w;
+    const int tile = t % p.num_tiles;
+    w.split = t / p.num_tiles;
+    tc_tile_coords(tile, p, w.mb, w.nb);
+    w.kb_begin = w.split * p.kb_per_split;
+    w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
+    return w;
 }
 
 struct TcWatch {
@@ -258,7 +282,7 @@ __device__ __forceinline__ void tc_strip_to_smem(uint32_t taddr, uint32_t stagin
     }
 }
 
-template <int CG, int BN, int STAGES, typename OutT, bool A_MN, bool B_MN>
+template <int CG, int BN, int STAGES, typename OutT, bool A_MN, bool B_MN, bool SPLIT = false>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p)
@@ -328,12 +352,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int s = 0; s < STAGES; ++s)
                 issued[s] = 0;
             bool ok = true;
-            for (int t = unit; ok && t < p.num_tiles; t += num_units) {
-                int mb, nb;
-                tc_tile_coords(t, p, mb, nb);
-                const int a_row = mb * TILE_M + static_cast<int>(rank) * TC_BM;
-                const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+            for (int t = unit; ok && t < p.num_work; t += num_units) {
+                const TcWork w = tc_work(t, p);
+                const int a_row = w.mb * TILE_M + static_cast<int>(rank) * TC_BM;
+                const int b_col = w.nb * BN + static_cast<int>(rank) * L::B_COLS;
+                for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     if (!tc_wait(empty_bar(stage), phase ^ 1, watch)) {
                         ok = false;
                         break;
@@ -398,7 +421,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t phase = 0;
             int local = 0;
             bool ok = true;
-            for (int t = unit; ok && t < p.num_tiles; t += num_units, ++local) {
+            for (int t = unit; ok && t < p.num_work; t += num_units, ++local) {
+                const TcWork w = tc_work(t, p);
                 const int acc = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 if (!tc_wait<CG == 2>(tempty_bar(acc), acc_phase ^ 1, watch)) {
@@ -407,7 +431,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     if (!tc_wait(full_bar(stage), phase, watch)) {
                         ok = false;
                         break;
@@ -426,7 +450,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bdesc = B_MN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
                                                     : smem_desc_sw128(b0 + k * 32, 16, 1024);
-                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, idesc, (kb != w.kb_begin) || k != 0);
                     }
                     if constexpr (CG == 2)
                         tc_commit_pair(empty_bar(stage), 0x3);
@@ -460,9 +484,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t leader_tempty1 = (CG == 2) ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
         int local = 0;
         uint32_t buf = 0;
-        for (int t = unit; t < p.num_tiles; t += num_units, ++local) {
-            int mb, nb;
-            tc_tile_coords(t, p, mb, nb);
+        for (int t = unit; t < p.num_work; t += num_units, ++local) {
+            const TcWork w = tc_work(t, p);
+            const int mb = w.mb, nb = w.nb;
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             int ok = 1;
@@ -491,7 +515,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tmC, stg, col0, row0);
+                    if constexpr (SPLIT)  // FP32 partial of split w.split (workspace)
+                        tma_store_3d(&tmC, stg, col0, row0, w.split);
+                    else
+                        tma_store_2d(&tmC, stg, col0, row0);
                     bulk_commit_group();
                 }
                 buf ^= 1;

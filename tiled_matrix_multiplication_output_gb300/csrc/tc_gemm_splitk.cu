@@ -1,0 +1,135 @@
+// Split-K for products with few output tiles and a long K: the K steps of
+// every output tile are divided into ranges, each range is a separate unit
+// of work for the persistent tensor-core kernel (so more SMs share the
+// reduction), its FP32 partial tile lands in a workspace, and a second
+// kernel adds the partials in split order -- a fixed order, so the result is
+// the same on every run -- and writes C.
+//
+// The reduction is a streaming pass over the workspace (HBM- or L2-bound):
+// it reads splits * M * N FP32 values and writes M * N outputs, 16 bytes of
+// workspace per thread and split in each step, grid-strided over the SMs.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tc_launch.cuh"
+
+namespace tmmo {
+namespace {
+
+__device__ __forceinline__ void store4(float* dst, float4 v)
+{
+    *reinterpret_cast<float4*>(dst) = v;
+}
+__device__ __forceinline__ void store4(__half* dst, float4 v)
+{
+    __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+    uint2 u = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    *reinterpret_cast<uint2*>(dst) = u;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 v)
+{
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    *reinterpret_cast<uint2*>(dst) = u;
+}
+
+__device__ __forceinline__ float4 load4(const float* src)
+{
+    return *reinterpret_cast<const float4*>(src);
+}
+__device__ __forceinline__ float4 load4(const __half* src)
+{
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* src)
+{
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// C[i] = alpha * sum_s ws[s][i] + beta * C[i], four elements per step
+// (M * N is a multiple of 4 because N is).
+template <typename OutT>
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ ws, OutT* C, long long mn, int splits,
+                         float alpha, float beta)
+{
+    const long long n4 = mn / 4;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += stride) {
+        float4 acc = load4(ws + 4 * i);
+        for (int s = 1; s < splits; ++s) {
+            const float4 v = load4(ws + static_cast<long long>(s) * mn + 4 * i);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        acc.x *= alpha;
+        acc.y *= alpha;
+        acc.z *= alpha;
+        acc.w *= alpha;
+        if (beta != 0.0f) {
+            const float4 c = load4(C + 4 * i);
+            acc.x = fmaf(beta, c.x, acc.x);
+            acc.y = fmaf(beta, c.y, acc.y);
+            acc.z = fmaf(beta, c.z, acc.z);
+            acc.w = fmaf(beta, c.w, acc.w);
+        }
+        store4(C + 4 * i, acc);
+    }
+}
+
+template <typename OutT>
+cudaError_t launch_reduce(const TcLaunch& l, int splits, cudaStream_t stream)
+{
+    const long long mn = static_cast<long long>(l.M) * l.N;
+    const long long n4 = mn / 4;
+    const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 8;
+    const int grid = static_cast<int>(std::max<long long>(1, std::min((n4 + 255) / 256, cap)));
+    splitk_reduce_kernel<OutT><<<grid, 256, 0, stream>>>(l.workspace, static_cast<OutT*>(l.C), mn,
+                                                        splits, l.alpha, l.beta);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int splitk_used_splits(int64_t K, int requested)
+{
+    const int64_t k_blocks = (K + TC_BK - 1) / TC_BK;
+    if (k_blocks <= 0)
+        return 1;
+    const int64_t s = std::max<int64_t>(1, std::min<int64_t>(requested, k_blocks));
+    const int64_t per = (k_blocks + s - 1) / s;
+    return static_cast<int>((k_blocks + per - 1) / per);
+}
+
+cudaError_t tc_splitk_launch(const TcLaunch& l, int* used_splits, cudaStream_t stream)
+{
+    const int splits = splitk_used_splits(l.K, l.k_splits);
+    TcLaunch k = l;
+    k.k_splits = splits;
+    k.alpha = 1.0f;  // alpha and beta are applied by the reduction
+    k.beta = 0.0f;
+    cudaError_t err = launch_variant<1, 128, 6, float, false, true, true>(k, stream);
+    if (err != cudaSuccess)
+        return err;
+    if (used_splits)
+        *used_splits = splits;
+    switch (l.out_dtype) {
+    case DT_F32:
+        return launch_reduce<float>(l, splits, stream);
+    case DT_F16:
+        return launch_reduce<__half>(l, splits, stream);
+    default:
+        return launch_reduce<__nv_bfloat16>(l, splits, stream);
+    }
+}
+
+}  // namespace tmmo

@@ -59,12 +59,31 @@ bool encode_2d(CUtensorMap* map, int dt, const void* base, uint64_t rows, uint64
     return r == CUDA_SUCCESS;
 }
 
-template <int CG, int BN, int STAGES, typename OutT, bool A_MN, bool B_MN>
+// FP32 split-K workspace [splits][rows][cols] as a 3-D tensor map with boxes
+// of 32 rows x 32 columns x 1 split, 128-byte swizzle.
+bool encode_workspace(CUtensorMap* map, float* base, uint64_t splits, uint64_t rows,
+                      uint64_t cols)
+{
+    auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {cols, rows, splits};
+    const cuuint64_t strides[2] = {cols * 4, rows * cols * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int CG, int BN, int STAGES, typename OutT, bool A_MN, bool B_MN, bool SPLIT = false>
 cudaError_t launch_variant(const TcLaunch& l, cudaStream_t stream)
 {
     using L = TcLayout<CG, BN, STAGES>;
     constexpr int STRIP = TcOut<OutT>::STRIP;
-    auto kern = tc_gemm_kernel<CG, BN, STAGES, OutT, A_MN, B_MN>;
+    static_assert(!SPLIT || sizeof(OutT) == 4, "split-K partials are FP32");
+    auto kern = tc_gemm_kernel<CG, BN, STAGES, OutT, A_MN, B_MN, SPLIT>;
 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -117,7 +136,13 @@ cudaError_t launch_variant(const TcLaunch& l, cudaStream_t stream)
                            : encode_2d(&ta, l.in_dtype, l.A, l.M, l.K, TC_BM, TC_BK);
     const bool ok_b = B_MN ? encode_2d(&tb, l.in_dtype, l.B, l.K, l.N, TC_BK, 64)
                            : encode_2d(&tb, l.in_dtype, l.B, l.N, l.K, BN / CG, TC_BK);
-    if (!ok_a || !ok_b || !encode_2d(&tc, l.out_dtype, l.C, l.M, l.N, 32, STRIP))
+    const int k_blocks = (l.K + TC_BK - 1) / TC_BK;
+    const int splits = SPLIT ? std::max(1, std::min(l.k_splits, k_blocks)) : 1;
+    const int kb_per_split = (k_blocks + splits - 1) / splits;
+    const int used_splits = (k_blocks + kb_per_split - 1) / kb_per_split;  // none empty
+    const bool ok_c = SPLIT ? encode_workspace(&tc, l.workspace, used_splits, l.M, l.N)
+                            : encode_2d(&tc, l.out_dtype, l.C, l.M, l.N, 32, STRIP);
+    if (!ok_a || !ok_b || !ok_c)
         return cudaErrorNotSupported;
 
     TcParams p{};
@@ -127,7 +152,10 @@ cudaError_t launch_variant(const TcLaunch& l, cudaStream_t stream)
     p.tiles_m = (l.M + TC_BM * CG - 1) / (TC_BM * CG);
     p.tiles_n = (l.N + BN - 1) / BN;
     p.num_tiles = p.tiles_m * p.tiles_n;
-    p.k_blocks = (l.K + TC_BK - 1) / TC_BK;
+    p.k_blocks = k_blocks;
+    p.k_splits = used_splits;
+    p.kb_per_split = kb_per_split;
+    p.num_work = p.num_tiles * used_splits;
     p.group_m = TMMO_RASTER_GROUP;
     p.idesc = tc_idesc(l.in_dtype == DT_BF16, TC_BM * CG, BN, A_MN, B_MN);
     p.status = l.status;
@@ -137,7 +165,7 @@ cudaError_t launch_variant(const TcLaunch& l, cudaStream_t stream)
     p.alpha = l.alpha;
     p.beta = l.beta;
 
-    const int units = std::max(1, std::min(p.num_tiles, units_cap));
+    const int units = std::max(1, std::min(p.num_work, units_cap));
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -12,6 +12,9 @@ struct TcParams {
     int M, N, K;
     int tiles_m, tiles_n, num_tiles;  // output tiles of (128 * CG) x BN
     int k_blocks;                      // ceil(K / 64)
+    int k_splits;                      // K ranges per tile (1 = no split-K)
+    int kb_per_split;                  // K steps per range
+    int num_work;                      // num_tiles * k_splits units of work
     int group_m;                       // raster group height, in tile rows
     uint32_t idesc;                    // tcgen05 instruction descriptor
     int* status;                       // device status word (never null)
