@@ -176,6 +176,39 @@ int gemm_splitk(const void* A, const void* B, void* C, int64_t M, int64_t N, int
                 gemm_dtype_t out_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gemm_splitk_noalloc -- gemm_splitk for callers that cannot allocate
+ * device memory; it allocates nothing.  The pages have no counterpart: this
+ * entry point exists for deployment, not for the method.
+ *
+ * Who needs it: code whose product is recorded into a CUDA graph or runs
+ * inside a framework that owns every allocation, real-time paths where a
+ * cudaMalloc (which may synchronize the device) is not allowed, and
+ * services that reserve all device memory up front.  Instead of a caller
+ * workspace, the FP32 partials live in one fixed array inside the library,
+ * GEMM_SPLITK_NOALLOC_MAX_BYTES on every GPU that loads the library, kept
+ * until the process exits.
+ *
+ * Limits and rules:
+ *  - gemm_splitk_workspace_size(M, N, K, splits) must not exceed
+ *    GEMM_SPLITK_NOALLOC_MAX_BYTES; larger requests return
+ *    GEMM_ERR_UNSUPPORTED and launch nothing (use fewer splits, or
+ *    gemm_splitk with your own workspace).
+ *  - Every call shares the one array and the array keeps the last call's
+ *    partials; nothing in it needs to start at zero (each call overwrites
+ *    every partial it reads).  Calls whose work overlaps on the GPU -- on
+ *    different streams, or on different host threads -- race on the array
+ *    and give wrong results; serialize them (one stream is enough).
+ *  - The first call on each device looks up the array's device address;
+ *    make that first call before any stream capture.
+ * Arguments, results, fallback for operands the tensor-core kernels cannot
+ * take, and other errors as gemm_splitk.
+ */
+#define GEMM_SPLITK_NOALLOC_MAX_BYTES ((size_t)8 << 20) /* 8 MiB of FP32 partials */
+int gemm_splitk_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                        int splits, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                        gemm_dtype_t out_dtype, void* stream);
+
+/*
  * gemm_select_kernel -- the kernel gemm_ex would launch for these arguments
  * on the current device (a gemm_kernel_t), or a negative gemm_status_t when
  * the arguments are invalid or unsupported.  Nothing is launched.

@@ -53,6 +53,7 @@ _SIGNATURES = {
     "gemm_splitk_workspace_size": ([_i64, _i64, _i64, _int], ctypes.c_size_t),
     "gemm_splitk": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _int, _p, ctypes.c_size_t,
                      _p], _int),
+    "gemm_splitk_noalloc": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _int, _p], _int),
     "gemm_device_status": ([_p], _int),
     "gemm_debug_config": ([_i64, _int], _int),
     "gemm_error_string": ([_int], ctypes.c_char_p),
@@ -135,6 +136,16 @@ def gemm_splitk(A, B, C, M, N, K, splits, in_dtype, acc_dtype, out_dtype, worksp
                 workspace_bytes, stream=None) -> int:
     return load_library().gemm_splitk(A, B, C, M, N, K, splits, in_dtype, acc_dtype, out_dtype,
                                       workspace, workspace_bytes, stream)
+
+
+# Size of the library's fixed split-K scratch (GEMM_SPLITK_NOALLOC_MAX_BYTES).
+SPLITK_NOALLOC_MAX_BYTES = 8 << 20
+
+
+def gemm_splitk_noalloc(A, B, C, M, N, K, splits, in_dtype, acc_dtype, out_dtype,
+                        stream=None) -> int:
+    return load_library().gemm_splitk_noalloc(A, B, C, M, N, K, splits, in_dtype, acc_dtype,
+                                              out_dtype, stream)
 
 
 def matmul_splitk(A, B, splits: int, out_dtype=None, workspace=None, stream=None):

@@ -393,3 +393,99 @@ extern "C" const char* gemm_error_string(int status)
         return "unknown status";
     }
 }
+
+// ------------------------------------------------------------------------
+// Split-K without any allocation.
+//
+// Some callers cannot allocate device memory at the point where they need a
+// product: code recorded into a CUDA graph or running under a framework that
+// owns every allocation, real-time paths that must not call cudaMalloc (it
+// can synchronize the device and take milliseconds), and memory-budgeted
+// services that reserve all device memory up front.  For them,
+// gemm_splitk_noalloc keeps its FP32 partials in the library's own
+// fixed-size device array below instead of a caller workspace.
+namespace tmmo {
+namespace {
+
+// The scratch of gemm_splitk_noalloc: GEMM_SPLITK_NOALLOC_MAX_BYTES on every
+// device that loads the library, held until the process exits.  Host code
+// must not use the symbol itself as a device address; it takes the address
+// from cudaGetSymbolAddress for the current device.
+static __device__ __align__(256) float g_splitk_scratch[GEMM_SPLITK_NOALLOC_MAX_BYTES / 4];
+
+float* g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// The device address of g_splitk_scratch on the current device, looked up
+// once per device (the first call on a device does the lookup).
+cudaError_t scratch_address(float** out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        float* p = nullptr;
+        err = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_splitk_scratch);
+        if (err != cudaSuccess)
+            return err;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace tmmo
+
+extern "C" int gemm_splitk_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                                   int64_t K, int splits, gemm_dtype_t in_dtype,
+                                   gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype, void* stream)
+{
+    const Problem q = plain(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype);
+    int rc = validate_problem(q);
+    if (rc != GEMM_OK)
+        return rc;
+    if (splits < 1)
+        return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!tc_eligible(q))
+        return run(q, GEMM_KERNEL_AUTO, s);  // these kernels use no scratch
+    if (gemm_splitk_workspace_size(M, N, K, splits) > GEMM_SPLITK_NOALLOC_MAX_BYTES)
+        return GEMM_ERR_UNSUPPORTED;  // the partials do not fit the fixed scratch
+    float* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    TcLaunch l{};
+    l.variant = TC_128x128;
+    l.op_a = GEMM_OP_N;
+    l.op_b = GEMM_OP_N;
+    l.alpha = 1.0f;
+    l.beta = 0.0f;
+    l.in_dtype = in_dtype;
+    l.out_dtype = out_dtype;
+    l.A = A;
+    l.B = B;
+    l.C = C;
+    l.M = static_cast<int>(M);
+    l.N = static_cast<int>(N);
+    l.K = static_cast<int>(K);
+    l.num_sms = d.num_sms;
+    l.status = d.status;
+    l.wait_budget = g_wait_budget.load();
+    l.fault_skip_kblock = g_fault_skip_kblock.load();
+    l.k_splits = splits;
+    l.workspace = scratch;
+    cudaError_t err = tc_splitk_launch(l, nullptr, s);
+    if (err == cudaErrorNotSupported)
+        return GEMM_ERR_UNSUPPORTED;
+    return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
