@@ -143,6 +143,34 @@ int gemm_general(const void* A, const void* B, void* C, int64_t M, int64_t N, in
                  void* stream);
 
 /*
+ * gemm_workspace_size -- bytes of workspace gemm_ex_ws can use for these
+ * sizes on the current device (an upper bound: one 256 x 256 FP32 tile per
+ * pair of SMs), or 0 for empty products or when no device is available.
+ */
+size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * gemm_ex_ws -- gemm_ex with a workspace that evens out the last wave.
+ *
+ * The persistent kernel runs the output tiles in waves of one tile per CTA
+ * pair.  When the tile count is not a multiple of the pairs resident on the
+ * GPU, the last wave leaves pairs idle; with a workspace, the tiles of that
+ * last wave are instead split along K into as many pieces as there are idle
+ * pairs, their FP32 partials go to `workspace` (caller-owned device memory,
+ * 16-byte aligned; gemm_workspace_size bytes always suffice), and a second
+ * kernel on the same stream adds each tile's pieces in K order and writes
+ * it.  The result differs from gemm_ex's only in the summation order of those
+ * tiles, and is identical run to run.  Without a workspace (NULL), with one
+ * too small for the plan, or when the automatic choice is not the CTA-pair
+ * kernel, this is gemm_ex.  Calls sharing a workspace must not overlap in
+ * time.  Errors as gemm_ex, plus GEMM_ERR_INVALID_VALUE for a misaligned
+ * workspace.
+ */
+int gemm_ex_ws(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+               gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gemm_splitk_workspace_size -- bytes of FP32 workspace gemm_splitk needs:
  * used_splits * M * N * 4, where used_splits <= splits is the number of
  * equal ranges of 64-wide K steps K is divided into (no range is empty).

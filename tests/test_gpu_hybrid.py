@@ -1,0 +1,83 @@
+"""gemm_ex_ws: the persistent CTA-pair kernel with the tiles of its last,
+partial wave split along K (FP32 partials in a caller workspace, summed in K
+order by a second kernel).  Exact on integer inputs, within the bound on the
+full-size workloads, identical run to run, and equal to gemm_ex wherever the
+plan does not split."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_matrix_multiplication_output_gb300 as tg
+from tests.helpers import expect_exact, sample_indices
+from tiled_matrix_multiplication_output_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    tg.gemm_debug_config(0, -1)
+
+
+def _ws(A, B, out_dtype=torch.float32, workspace=None):
+    C = tg.matmul_ws(A.cuda(), B.cuda(), out_dtype=out_dtype, workspace=workspace)
+    assert tg.gemm_device_status(torch.cuda.current_stream().cuda_stream) == 0
+    return C.cpu()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_split_last_wave_exact_integers(out_dtype):
+    """2560 x 2560: 100 pair tiles over the resident pairs leaves a partial
+    last wave, which is split; ragged K (520 = 8 * 64 + 8)."""
+    A, B = inputs.draw(2560, 2560, 520, "bf16", "int", seed=90)
+    expect_exact(_ws(A, B, out_dtype), A, B)
+
+
+def test_ragged_edges_exact():
+    A, B = inputs.draw(2400, 2504, 776, "f16", "int", seed=91)
+    expect_exact(_ws(A, B), A, B)
+
+
+@pytest.mark.parametrize("name", ["square_4096_f16", "square_8192_bf16"])
+def test_full_size_workloads(name):
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.make(w)
+    odt = binding.torch_dtype(w.out_dtype)
+    C = _ws(A, B, odt)
+    rows, cols = sample_indices(w.M, w.N, 3000, seed=w.seed + 10, tile_m=256, tile_n=256)
+    # the split tiles are the last tiles in raster order: sample them densely
+    tail_r = np.random.default_rng(1).integers(w.M - 2048, w.M, 2000)
+    tail_c = np.random.default_rng(2).integers(0, w.N, 2000)
+    rows = np.concatenate([rows, tail_r]); cols = np.concatenate([cols, tail_c])
+    ref, ref_abs = oracle.gemm_entries(A, B, rows, cols)
+    got = C[torch.from_numpy(rows), torch.from_numpy(cols)].double().numpy()
+    assert np.all(np.abs(got - ref) <= oracle.tolerance(ref_abs))
+    C2 = _ws(A, B, odt)
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+
+
+def test_small_or_missing_workspace_falls_back():
+    A, B = inputs.draw(2560, 2560, 256, "bf16", "int", seed=92)
+    tiny = torch.empty(64, dtype=torch.uint8, device="cuda")
+    expect_exact(_ws(A, B, workspace=tiny), A, B)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(2560, 2560, device="cuda")
+    rc = tg.gemm_ex_ws(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), 2560, 2560, 256, tg.BF16,
+                       tg.F32, tg.F32, None, 0, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    expect_exact(C.cpu(), A, B)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    rc = tg.gemm_ex_ws(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), 2560, 2560, 256, tg.BF16,
+                       tg.F32, tg.F32, ws.data_ptr() + 4, 1 << 19, None)
+    assert rc == tg.binding.ERR_INVALID_VALUE
+
+
+def test_workspace_size_bound():
+    n = tg.gemm_workspace_size(8192, 8192, 8192)
+    props = torch.cuda.get_device_properties(0)
+    assert n == (props.multi_processor_count // 2) * 256 * 256 * 4
+    assert tg.gemm_workspace_size(0, 8, 8) == 0

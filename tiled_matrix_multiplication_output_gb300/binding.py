@@ -50,6 +50,9 @@ _SIGNATURES = {
     "gemm_general": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, ctypes.c_float, ctypes.c_float,
                       _int, _int, _int, _int, _p], _int),
     "gemm_ex_host": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, _p, _p, _p], _int),
+    "gemm_workspace_size": ([_i64, _i64, _i64], ctypes.c_size_t),
+    "gemm_ex_ws": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, ctypes.c_size_t, _p],
+                   _int),
     "gemm_splitk_workspace_size": ([_i64, _i64, _i64, _int], ctypes.c_size_t),
     "gemm_splitk": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _int, _p, ctypes.c_size_t,
                      _p], _int),
@@ -126,6 +129,36 @@ def gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype
                  stream=None) -> int:
     return load_library().gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype,
                                        out_dtype, dA, dB, dC, stream)
+
+
+def gemm_workspace_size(M, N, K) -> int:
+    return load_library().gemm_workspace_size(M, N, K)
+
+
+def gemm_ex_ws(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, workspace, workspace_bytes,
+               stream=None) -> int:
+    return load_library().gemm_ex_ws(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, workspace,
+                                     workspace_bytes, stream)
+
+
+def matmul_ws(A, B, out_dtype=None, workspace=None, out=None, stream=None):
+    """C = A @ B through gemm_ex_ws (last-wave balancing with a workspace,
+    allocated by PyTorch unless given)."""
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[1]
+    odt = torch.float32 if out_dtype is None else (
+        torch_dtype(out_dtype) if isinstance(out_dtype, (str, int)) else out_dtype)
+    C = out if out is not None else torch.empty((M, N), dtype=odt, device=A.device)
+    if workspace is None:
+        workspace = torch.empty(max(gemm_workspace_size(M, N, K), 16), dtype=torch.uint8,
+                                device=A.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = gemm_ex_ws(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, dtype_code(A.dtype), F32,
+                    dtype_code(C.dtype), workspace.data_ptr(), nbytes, _stream_handle(stream))
+    if rc != OK:
+        raise GemmError(rc, "gemm_ex_ws")
+    return C
 
 
 def gemm_splitk_workspace_size(M, N, K, splits) -> int:

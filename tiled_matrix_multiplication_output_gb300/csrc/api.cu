@@ -319,6 +319,62 @@ extern "C" int gemm_splitk(const void* A, const void* B, void* C, int64_t M, int
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+extern "C" size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0)
+        return 0;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return 0;
+    // At most one split piece per resident CTA pair, each a 256 x 256 FP32 tile.
+    return static_cast<size_t>(d.num_sms / 2) * 256u * 256u * 4u;
+}
+
+extern "C" int gemm_ex_ws(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                          gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
+                          void* workspace, size_t workspace_bytes, void* stream)
+{
+    const Problem q = plain(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype);
+    int rc = validate_problem(q);
+    if (rc != GEMM_OK)
+        return rc;
+    if (M == 0 || N == 0)
+        return GEMM_OK;
+    if (workspace && !aligned16(workspace))
+        return GEMM_ERR_INVALID_VALUE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    const int kernel = auto_kernel(q, d.num_sms);
+    if (kernel != GEMM_KERNEL_TC_256x256 || !workspace)
+        return run(q, kernel, s);
+    TcLaunch l{};
+    l.variant = TC_256x256;
+    l.op_a = GEMM_OP_N;
+    l.op_b = GEMM_OP_N;
+    l.alpha = 1.0f;
+    l.beta = 0.0f;
+    l.in_dtype = in_dtype;
+    l.out_dtype = out_dtype;
+    l.A = A;
+    l.B = B;
+    l.C = C;
+    l.M = static_cast<int>(M);
+    l.N = static_cast<int>(N);
+    l.K = static_cast<int>(K);
+    l.num_sms = d.num_sms;
+    l.status = d.status;
+    l.wait_budget = g_wait_budget.load();
+    l.fault_skip_kblock = g_fault_skip_kblock.load();
+    l.workspace = static_cast<float*>(workspace);
+    l.workspace_bytes = workspace_bytes;
+    cudaError_t err = tc_hybrid_launch(l, s);
+    if (err == cudaErrorNotSupported)
+        return GEMM_ERR_UNSUPPORTED;
+    return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
                             int64_t N, int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
                             gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* stream)

@@ -42,8 +42,47 @@ struct TcLaunch {
     long long wait_budget;
     int fault_skip_kblock;
     int k_splits;       // split-K only: requested K ranges per tile
-    float* workspace;   // split-K only: [k_splits][M][N] FP32 partials
+    float* workspace;   // split-K: [k_splits][M][N] FP32 partials; hybrid: tail partials
+    size_t workspace_bytes;  // hybrid only: capacity of workspace
+    bool hybrid;        // split the tiles of the last, partial wave along K
+    int* plan;          // if set, receives the work plan (see tc_launch.cuh)
 };
+
+// Hybrid plan for `tiles` output tiles on `units` resident CTAs (or pairs)
+// with `k_blocks` K steps: whole waves of tiles stay whole; the r tiles of
+// the last, partial wave are each split into `splits` K ranges so that the
+// r * splits pieces occupy the idle units.  Splitting is used only when it
+// gives at least two ranges of at least four K steps.
+inline void hybrid_plan(int tiles, int units, int k_blocks, int* dp_tiles, int* splits,
+                        int* kb_per_split)
+{
+    *dp_tiles = tiles;
+    *splits = 1;
+    *kb_per_split = k_blocks;
+    if (units <= 0 || tiles <= units)
+        return;
+    const int r = tiles % units;
+    if (r == 0)
+        return;
+    int s = units / r;
+    if (s > k_blocks / 4)
+        s = k_blocks / 4;
+    if (s < 2)
+        return;
+    const int per = (k_blocks + s - 1) / s;
+    *dp_tiles = tiles - r;
+    *splits = (k_blocks + per - 1) / per;
+    *kb_per_split = per;
+}
+
+// Hybrid product on the CTA-pair kernel (operands as stored): launches the
+// tensor-core kernel with the hybrid plan, then, if tiles were split, the
+// reduction of their partials into C.
+cudaError_t tc_hybrid_launch(const TcLaunch& l, cudaStream_t stream);
+
+// Sums the split partials of the tail tiles described by plan[] (as filled
+// by the tensor-core launch) into C, applying alpha and beta.
+cudaError_t tail_reduce_launch(const TcLaunch& l, const int* plan, cudaStream_t stream);
 
 // Encodes the tensor maps and launches; returns cudaSuccess, a CUDA error, or
 // cudaErrorNotSupported when the driver entry point for tensor maps is

@@ -114,22 +114,42 @@ __device__ __forceinline__ void tc_tile_coords(int t, const TcParams& p, int& mb
 }
 
 // One unit of work: an output tile and the range of K steps it accumulates.
-// Without split-K (k_splits = 1) a unit is a whole tile; with split-K, unit
-// t covers tile t % num_tiles over K split t / num_tiles.
+// Units t < dp_tiles are whole tiles (tile t, all of K), written to C.  The
+// remaining units split the last num_tiles - dp_tiles tiles along K into
+// k_splits ranges each (unit dp_tiles + j: tile dp_tiles + j / k_splits,
+// range j % k_splits); their FP32 partials go to a workspace and are summed
+// by a second kernel.  dp_tiles = num_tiles is the plain product, dp_tiles =
+// 0 is split-K, anything between fills the last, partial wave of tiles with
+// split pieces so that every CTA finishes at about the same time.
 struct TcWork {
     int mb, nb;
     int kb_begin, kb_end;
-    int split;
+    int split;    // K range within the tile
+    int slot;     // index of the partial among all split units
+    bool partial;
 };
 
 __device__ __forceinline__ TcWork tc_work(int t, const TcParams& p)
 {
     TcWork w;
-    const int tile = t % p.num_tiles;
-    w.split = t / p.num_tiles;
+    int tile;
+    if (t < p.dp_tiles) {
+        tile = t;
+        w.split = 0;
+        w.slot = 0;
+        w.partial = false;
+        w.kb_begin = 0;
+        w.kb_end = p.k_blocks;
+    } else {
+        const int j = t - p.dp_tiles;
+        tile = p.dp_tiles + j / p.k_splits;
+        w.split = j % p.k_splits;
+        w.slot = j;
+        w.partial = true;
+        w.kb_begin = w.split * p.kb_per_split;
+        w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
+    }
     tc_tile_coords(tile, p, w.mb, w.nb);
-    w.kb_begin = w.split * p.kb_per_split;
-    w.kb_end = min(p.k_blocks, w.kb_begin + p.kb_per_split);
     return w;
 }
 
@@ -285,7 +305,8 @@ __device__ __forceinline__ void tc_strip_to_smem(uint32_t taddr, uint32_t stagin
 template <int CG, int BN, int STAGES, typename OutT, bool A_MN, bool B_MN, bool SPLIT = false>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const TcParams p)
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
+                   const TcParams p)
 {
     using L = TcLayout<CG, BN, STAGES>;
     constexpr int STRIP = TcOut<OutT>::STRIP;
@@ -327,6 +348,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmC);
+        tma_prefetch_desc(&tmW);
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_u32(tmem_slot), L::TMEM_COLS);
@@ -484,6 +506,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t leader_tempty1 = (CG == 2) ? mapa_shared(tempty_bar(1), 0) : tempty_bar(1);
         int local = 0;
         uint32_t buf = 0;
+        TcParams p_raw = p;  // partial tiles are stored unscaled
+        p_raw.alpha = 1.0f;
+        p_raw.beta = 0.0f;
         for (int t = unit; t < p.num_work; t += num_units, ++local) {
             const TcWork w = tc_work(t, p);
             const int mb = w.mb, nb = w.nb;
@@ -499,8 +524,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int row0 = mb * TILE_M + static_cast<int>(rank) * TC_BM + q * 32;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
+            if (!SPLIT && w.partial) {
+                // Tail piece: the whole TILE_M x BN FP32 partial goes to
+                // workspace slot w.slot (tile-local rows and columns; the
+                // reduction clips to C).
+                const int trow = static_cast<int>(rank) * TC_BM + q * 32;
 #pragma unroll 1
-            for (int s = 0; s < BN / STRIP; ++s) {
+                for (int s = 0; s < BN / 32; ++s) {
+                    const uint32_t stg = staging0 + buf * TC_STAGING_BYTES;
+                    if (lane == 0)
+                        bulk_wait_group_read<1>();
+                    __syncwarp();
+                    tc_strip_to_smem<float>(t_row + s * 32, stg, lane, p_raw, 0, 0);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tmW, stg, s * 32, trow, w.slot);
+                        bulk_commit_group();
+                    }
+                    buf ^= 1;
+                }
+            }
+#pragma unroll 1
+            for (int s = 0; s < BN / STRIP && (SPLIT || !w.partial); ++s) {
                 const int col0 = nb * BN + s * STRIP;
                 if (row0 >= p.M || col0 >= p.N)
                     break;  // the rest of this warp's strips lie wholly outside C

@@ -98,7 +98,85 @@ cudaError_t launch_reduce(const TcLaunch& l, int splits, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+// Tail reduction of the hybrid plan: block (x = tail tile, y = band of 16
+// rows) sums the `splits` FP32 partials of its tile rows in split order and
+// writes the part of C inside M x N, four columns per thread and step.
+template <typename OutT>
+__global__ void __launch_bounds__(256)
+    tail_reduce_kernel(const float* __restrict__ ws, OutT* C, TcParams p, int tile_m, int tile_n,
+                       int splits)
+{
+    const int tail = blockIdx.x;
+    int mb, nb;
+    tc_tile_coords(p.dp_tiles + tail, p, mb, nb);
+    const long long tile_elems = static_cast<long long>(tile_m) * tile_n;
+    const float* base = ws + static_cast<long long>(tail) * splits * tile_elems;
+    const int groups_per_row = tile_n / 4;
+    const int band_rows = 16;
+    for (int g = threadIdx.x; g < band_rows * groups_per_row; g += blockDim.x) {
+        const int r = blockIdx.y * band_rows + g / groups_per_row;
+        const int c = (g % groups_per_row) * 4;
+        const int grow = mb * tile_m + r;
+        const int gcol = nb * tile_n + c;
+        if (r >= tile_m || grow >= p.M || gcol >= p.N)
+            continue;  // N is a multiple of 4, so a group lies wholly inside or outside
+        const long long off = static_cast<long long>(r) * tile_n + c;
+        float4 acc = load4(base + off);
+        for (int s = 1; s < splits; ++s) {
+            const float4 v = load4(base + static_cast<long long>(s) * tile_elems + off);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        acc.x *= p.alpha;
+        acc.y *= p.alpha;
+        acc.z *= p.alpha;
+        acc.w *= p.alpha;
+        OutT* dst = C + static_cast<long long>(grow) * p.N + gcol;
+        if (p.beta != 0.0f) {
+            const float4 cv = load4(dst);
+            acc.x = fmaf(p.beta, cv.x, acc.x);
+            acc.y = fmaf(p.beta, cv.y, acc.y);
+            acc.z = fmaf(p.beta, cv.z, acc.z);
+            acc.w = fmaf(p.beta, cv.w, acc.w);
+        }
+        store4(dst, acc);
+    }
+}
+
+template <typename OutT>
+cudaError_t launch_tail(const TcLaunch& l, const int* plan, cudaStream_t stream)
+{
+    TcParams p{};
+    p.M = l.M;
+    p.N = l.N;
+    p.dp_tiles = plan[0];
+    p.tiles_m = plan[3];
+    p.tiles_n = plan[4];
+    p.group_m = plan[5];
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.alpha = l.alpha;
+    p.beta = l.beta;
+    const dim3 grid(plan[2], (plan[6] + 15) / 16, 1);
+    tail_reduce_kernel<OutT><<<grid, 256, 0, stream>>>(l.workspace, static_cast<OutT*>(l.C), p,
+                                                       plan[6], plan[7], plan[1]);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t tail_reduce_launch(const TcLaunch& l, const int* plan, cudaStream_t stream)
+{
+    switch (l.out_dtype) {
+    case DT_F32:
+        return launch_tail<float>(l, plan, stream);
+    case DT_F16:
+        return launch_tail<__half>(l, plan, stream);
+    default:
+        return launch_tail<__nv_bfloat16>(l, plan, stream);
+    }
+}
 
 int splitk_used_splits(int64_t K, int requested)
 {

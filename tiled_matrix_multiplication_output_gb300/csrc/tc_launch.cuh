@@ -137,25 +137,60 @@ cudaError_t launch_variant(const TcLaunch& l, cudaStream_t stream)
     const bool ok_b = B_MN ? encode_2d(&tb, l.in_dtype, l.B, l.K, l.N, TC_BK, 64)
                            : encode_2d(&tb, l.in_dtype, l.B, l.N, l.K, BN / CG, TC_BK);
     const int k_blocks = (l.K + TC_BK - 1) / TC_BK;
-    const int splits = SPLIT ? std::max(1, std::min(l.k_splits, k_blocks)) : 1;
-    const int kb_per_split = (k_blocks + splits - 1) / splits;
-    const int used_splits = (k_blocks + kb_per_split - 1) / kb_per_split;  // none empty
-    const bool ok_c = SPLIT ? encode_workspace(&tc, l.workspace, used_splits, l.M, l.N)
+    const int tiles_m = (l.M + TC_BM * CG - 1) / (TC_BM * CG);
+    const int tiles_n = (l.N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+    // Work plan: split-K splits every tile; the hybrid plan runs whole waves
+    // of tiles and splits only the tiles of the last, partial wave (when that
+    // helps and the workspace can hold their partials); otherwise all tiles
+    // are whole.
+    int dp_tiles = num_tiles, splits = 1, kb_per_split = k_blocks;
+    if (SPLIT) {
+        dp_tiles = 0;
+        splits = std::max(1, std::min(l.k_splits, k_blocks));
+        kb_per_split = (k_blocks + splits - 1) / splits;
+        splits = (k_blocks + kb_per_split - 1) / kb_per_split;  // none empty
+    } else if (l.hybrid) {
+        hybrid_plan(num_tiles, std::min(num_tiles, units_cap), k_blocks, &dp_tiles, &splits,
+                    &kb_per_split);
+        const size_t need = static_cast<size_t>(num_tiles - dp_tiles) * splits * TC_BM * CG * BN * 4;
+        if (dp_tiles < num_tiles && (!l.workspace || l.workspace_bytes < need)) {
+            dp_tiles = num_tiles;
+            splits = 1;
+            kb_per_split = k_blocks;
+        }
+    }
+    const int slots = (num_tiles - dp_tiles) * splits;
+    const bool ok_c = SPLIT ? encode_workspace(&tc, l.workspace, splits, l.M, l.N)
                             : encode_2d(&tc, l.out_dtype, l.C, l.M, l.N, 32, STRIP);
+    CUtensorMap tw = tc;  // tail workspace: slots of TILE_M x BN FP32 partials
+    if (!SPLIT && slots > 0 && !encode_workspace(&tw, l.workspace, slots, TC_BM * CG, BN))
+        return cudaErrorNotSupported;
     if (!ok_a || !ok_b || !ok_c)
         return cudaErrorNotSupported;
+    if (l.plan) {
+        l.plan[0] = dp_tiles;
+        l.plan[1] = splits;
+        l.plan[2] = num_tiles - dp_tiles;
+        l.plan[3] = tiles_m;
+        l.plan[4] = tiles_n;
+        l.plan[5] = TMMO_RASTER_GROUP;
+        l.plan[6] = TC_BM * CG;
+        l.plan[7] = BN;
+    }
 
     TcParams p{};
     p.M = l.M;
     p.N = l.N;
     p.K = l.K;
-    p.tiles_m = (l.M + TC_BM * CG - 1) / (TC_BM * CG);
-    p.tiles_n = (l.N + BN - 1) / BN;
-    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.tiles_m = tiles_m;
+    p.tiles_n = tiles_n;
+    p.num_tiles = num_tiles;
     p.k_blocks = k_blocks;
-    p.k_splits = used_splits;
+    p.dp_tiles = dp_tiles;
+    p.k_splits = splits;
     p.kb_per_split = kb_per_split;
-    p.num_work = p.num_tiles * used_splits;
+    p.num_work = dp_tiles + slots;
     p.group_m = TMMO_RASTER_GROUP;
     p.idesc = tc_idesc(l.in_dtype == DT_BF16, TC_BM * CG, BN, A_MN, B_MN);
     p.status = l.status;
@@ -178,7 +213,7 @@ cudaError_t launch_variant(const TcLaunch& l, cudaStream_t stream)
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+    err = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tw, p);
     if (err != cudaSuccess)
         return err;
     return cudaGetLastError();

@@ -12,9 +12,10 @@ struct TcParams {
     int M, N, K;
     int tiles_m, tiles_n, num_tiles;  // output tiles of (128 * CG) x BN
     int k_blocks;                      // ceil(K / 64)
-    int k_splits;                      // K ranges per tile (1 = no split-K)
+    int dp_tiles;                      // tiles computed whole; the rest are split along K
+    int k_splits;                      // K ranges per split tile
     int kb_per_split;                  // K steps per range
-    int num_work;                      // num_tiles * k_splits units of work
+    int num_work;                      // dp_tiles + (num_tiles - dp_tiles) * k_splits units
     int group_m;                       // raster group height, in tile rows
     uint32_t idesc;                    // tcgen05 instruction descriptor
     int* status;                       // device status word (never null)
