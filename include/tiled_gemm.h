@@ -279,6 +279,13 @@ int gemm_device_status(void* stream);
  */
 int gemm_debug_config(int64_t wait_budget_cycles, int fault_skip_kblock);
 
+/*
+ * gemm_launch_count -- how many kernels the library has launched in this
+ * process so far (all devices and streams; a plain product is one launch,
+ * split-K and gemm_ex_ws with split tiles are two).  For accounting only.
+ */
+uint64_t gemm_launch_count(void);
+
 /* gemm_error_string -- a static description of a gemm_status_t. */
 const char* gemm_error_string(int status);
 

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "gemm_splitk_noalloc": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _int, _p], _int),
     "gemm_device_status": ([_p], _int),
     "gemm_debug_config": ([_i64, _int], _int),
+    "gemm_launch_count": ([], ctypes.c_uint64),
     "gemm_error_string": ([_int], ctypes.c_char_p),
 }
 
@@ -205,6 +206,10 @@ def matmul_splitk(A, B, splits: int, out_dtype=None, workspace=None, stream=None
 
 def gemm_device_status(stream=None) -> int:
     return load_library().gemm_device_status(stream)
+
+
+def gemm_launch_count() -> int:
+    return load_library().gemm_launch_count()
 
 
 def gemm_debug_config(wait_budget_cycles: int = 0, fault_skip_kblock: int = -1) -> int:

@@ -21,6 +21,7 @@ constexpr int kMaxDevices = 64;
 constexpr long long kDefaultWaitBudget = 2000000000LL;  // ~1 s of SM clock
 
 std::atomic<long long> g_wait_budget{kDefaultWaitBudget};
+std::atomic<unsigned long long> g_launches{0};
 std::atomic<int> g_fault_skip_kblock{-1};
 
 struct DeviceInfo {
@@ -213,6 +214,12 @@ Problem plain(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
 }
 
 }  // namespace
+
+void note_launch()
+{
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+}
+
 }  // namespace tmmo
 
 using namespace tmmo;
@@ -423,6 +430,11 @@ extern "C" int gemm_device_status(void* stream)
         return GEMM_ERR_TIMEOUT;
     }
     return GEMM_OK;
+}
+
+extern "C" uint64_t gemm_launch_count(void)
+{
+    return g_launches.load(std::memory_order_relaxed);
 }
 
 extern "C" int gemm_debug_config(int64_t wait_budget_cycles, int fault_skip_kblock)

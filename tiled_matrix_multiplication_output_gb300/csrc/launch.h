@@ -7,6 +7,10 @@
 
 namespace tmmo {
 
+// Counts one launch of a library kernel (process-wide, all devices); read
+// through gemm_launch_count().
+void note_launch();
+
 // Internal dtype codes; they match gemm_dtype_t.
 enum { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 

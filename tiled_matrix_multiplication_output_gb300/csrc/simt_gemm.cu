@@ -147,6 +147,7 @@ cudaError_t launch_simt(const SimtLaunch& l, cudaStream_t stream)
     // Enough blocks for several resident per SM; each strides over tiles.
     const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 16;
     const int grid = static_cast<int>(std::max<long long>(1, std::min(tiles, cap)));
+    note_launch();
     simt_gemm_kernel<BM, BN, BK, TM, TN, InT, OutT><<<grid, NT, 0, stream>>>(
         static_cast<const InT*>(l.A), static_cast<const InT*>(l.B), static_cast<OutT*>(l.C), l.M,
         l.N, l.K, l.op_a, l.op_b, l.alpha, l.beta);

@@ -93,6 +93,7 @@ cudaError_t launch_reduce(const TcLaunch& l, int splits, cudaStream_t stream)
     const long long n4 = mn / 4;
     const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 8;
     const int grid = static_cast<int>(std::max<long long>(1, std::min((n4 + 255) / 256, cap)));
+    note_launch();
     splitk_reduce_kernel<OutT><<<grid, 256, 0, stream>>>(l.workspace, static_cast<OutT*>(l.C), mn,
                                                         splits, l.alpha, l.beta);
     return cudaGetLastError();
@@ -159,6 +160,7 @@ cudaError_t launch_tail(const TcLaunch& l, const int* plan, cudaStream_t stream)
     p.alpha = l.alpha;
     p.beta = l.beta;
     const dim3 grid(plan[2], (plan[6] + 15) / 16, 1);
+    note_launch();
     tail_reduce_kernel<OutT><<<grid, 256, 0, stream>>>(l.workspace, static_cast<OutT*>(l.C), p,
                                                        plan[6], plan[7], plan[1]);
     return cudaGetLastError();

@@ -213,6 +213,7 @@ cudaError_t launch_variant(const TcLaunch& l, cudaStream_t stream)
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    note_launch();
     err = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tw, p);
     if (err != cudaSuccess)
         return err;
