@@ -280,6 +280,24 @@ int gemm_device_status(void* stream);
 int gemm_debug_config(int64_t wait_budget_cycles, int fault_skip_kblock);
 
 /*
+ * gemm_traffic_model -- the tile-level traffic and working-set counts of the
+ * output-stationary loop nest ("Reading a matrix multiply through its
+ * tiles", sections "What fits in local storage?", "Count the repeated reads"
+ * and "Edge tiles still matter"), in closed form.  With no reuse of input
+ * tiles across output tiles and tm x tn x tk tiles, out[0..8] receive: A
+ * elements read M*K*ceil(N/tn); B elements read K*N*ceil(M/tm); C elements
+ * written M*N; their bytes (A and B at in_bytes, C at c_bytes); FLOPs
+ * 2*M*N*K; output tiles; tile steps along K; the largest per-step working
+ * set (actual extents of the first tile); and the working set of one full
+ * tm x tn x tk step (A, B tiles at in_bytes, accumulator at acc_bytes).  The
+ * automatic kernel choice ranks tile shapes with these counts.  Host-only;
+ * returns GEMM_ERR_INVALID_VALUE for negative sizes, non-positive tiles or a
+ * null out.
+ */
+int gemm_traffic_model(int64_t M, int64_t N, int64_t K, int64_t tm, int64_t tn, int64_t tk,
+                       int64_t in_bytes, int64_t acc_bytes, int64_t c_bytes, int64_t* out);
+
+/*
  * gemm_launch_count -- how many kernels the library has launched in this
  * process so far (all devices and streams; a plain product is one launch,
  * split-K and gemm_ex_ws with split tiles are two).  For accounting only.

@@ -68,3 +68,25 @@ def test_matmul_rejects_cpu_tensors(lib):
     import torch
     with pytest.raises(ValueError):
         tg.matmul(torch.zeros(2, 2), torch.zeros(2, 2))
+
+
+def test_library_traffic_model_matches_oracle_walker(lib):
+    """The library's closed-form counts (used by the kernel choice) equal the
+    oracle's tile-by-tile walk of the loop nest, edge tiles included."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(17)
+    cases = [(128, 128, 128, 16, 16, 32), (96, 200, 1000, 128, 128, 64),
+             (8192, 8192, 8192, 256, 256, 64), (1, 1, 1, 128, 256, 64)]
+    cases += [tuple(int(v) for v in rng.integers(1, 400, 3)) + tuple(int(v) for v in rng.integers(1, 80, 3))
+              for _ in range(150)]
+    for M, N, K, tm, tn, tk in cases:
+        for in_b, acc_b, c_b in ((2, 4, 4), (2, 4, 2), (4, 4, 4)):
+            got = tg.gemm_traffic_model(M, N, K, tm, tn, tk, in_b, acc_b, c_b)
+            want = oracle.traffic(M, N, K, tm, tn, tk, in_bytes=in_b, acc_bytes=acc_b, c_bytes=c_b)
+            assert got == want, (M, N, K, tm, tn, tk)
+
+
+def test_library_traffic_model_rejects_bad_tiles(lib):
+    with pytest.raises(tg.GemmError):
+        tg.gemm_traffic_model(8, 8, 8, 0, 8, 8)

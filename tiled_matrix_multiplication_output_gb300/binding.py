@@ -60,6 +60,7 @@ _SIGNATURES = {
     "gemm_device_status": ([_p], _int),
     "gemm_debug_config": ([_i64, _int], _int),
     "gemm_launch_count": ([], ctypes.c_uint64),
+    "gemm_traffic_model": ([_i64] * 9 + [_p], _int),
     "gemm_error_string": ([_int], ctypes.c_char_p),
 }
 
@@ -206,6 +207,20 @@ def matmul_splitk(A, B, splits: int, out_dtype=None, workspace=None, stream=None
 
 def gemm_device_status(stream=None) -> int:
     return load_library().gemm_device_status(stream)
+
+
+TRAFFIC_KEYS = ("a_elems", "b_elems", "c_elems", "bytes", "flops", "tiles", "steps",
+                "ws_max", "ws_full")
+
+
+def gemm_traffic_model(M, N, K, tm, tn, tk, in_bytes=2, acc_bytes=4, c_bytes=4) -> dict:
+    """The library's closed-form traffic / working-set counts as a dict."""
+    out = (ctypes.c_int64 * 9)()
+    rc = load_library().gemm_traffic_model(M, N, K, tm, tn, tk, in_bytes, acc_bytes, c_bytes,
+                                           out)
+    if rc != OK:
+        raise GemmError(rc, "gemm_traffic_model")
+    return dict(zip(TRAFFIC_KEYS, list(out)))
 
 
 def gemm_launch_count() -> int:

@@ -118,8 +118,10 @@ bool tc_eligible(const Problem& q)
 }
 
 // The automatic choice.  Tiny products go to the SIMT kernel (a tensor-core
-// launch has a fixed set-up cost); otherwise the largest tile that still
-// gives every SM work.
+// launch has a fixed set-up cost); otherwise the tensor-core variant with the
+// smallest predicted time: the tile traffic of the loop nest, the waves of
+// tiles over the resident CTAs and each tile shape's measured throughput
+// (predict_seconds in model.cu).
 int auto_kernel(const Problem& q, int num_sms)
 {
     const int64_t M = q.M, N = q.N, K = q.K;
@@ -128,13 +130,17 @@ int auto_kernel(const Problem& q, int num_sms)
     const double flops = 2.0 * double(M) * double(N) * double(K);
     if (flops < 2.0 * 64 * 64 * 64)
         return GEMM_KERNEL_SIMT;
-    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    if (pair_tiles >= num_sms / 2)
-        return GEMM_KERNEL_TC_256x256;
-    const int64_t wide_tiles = ((M + 127) / 128) * ((N + 255) / 256);
-    if (wide_tiles >= num_sms)
-        return GEMM_KERNEL_TC_128x256;
-    return GEMM_KERNEL_TC_128x128;
+    const int in_b = dt_size(q.in_dtype), out_b = dt_size(q.out_dtype);
+    int best = GEMM_KERNEL_TC_256x256;
+    double best_t = predict_seconds(M, N, K, TC_256x256, num_sms, in_b, out_b);
+    for (int v : {GEMM_KERNEL_TC_128x256, GEMM_KERNEL_TC_128x128}) {
+        const double t = predict_seconds(M, N, K, v, num_sms, in_b, out_b);
+        if (t < best_t * 0.98) {  // prefer the larger tile unless clearly slower
+            best_t = t;
+            best = v;
+        }
+    }
+    return best;
 }
 
 int validate_problem(const Problem& q)
@@ -429,6 +435,16 @@ extern "C" int gemm_device_status(void* stream)
             return GEMM_ERR_CUDA;
         return GEMM_ERR_TIMEOUT;
     }
+    return GEMM_OK;
+}
+
+extern "C" int gemm_traffic_model(int64_t M, int64_t N, int64_t K, int64_t tm, int64_t tn,
+                                  int64_t tk, int64_t in_bytes, int64_t acc_bytes, int64_t c_bytes,
+                                  int64_t* out)
+{
+    if (M < 0 || N < 0 || K < 0 || tm <= 0 || tn <= 0 || tk <= 0 || !out)
+        return GEMM_ERR_INVALID_VALUE;
+    traffic_model(M, N, K, tm, tn, tk, in_bytes, acc_bytes, c_bytes, out);
     return GEMM_OK;
 }
 

@@ -110,6 +110,16 @@ int splitk_used_splits(int64_t K, int requested);
 // cuTensorMapEncodeTiled from the driver (as void*), or null if unavailable.
 void* tensor_map_encoder();
 
+// Closed-form tile traffic and working set of the output-stationary loop nest
+// (element counts of A, B, C; bytes; FLOPs; tiles; K steps; largest and full
+// per-step working set in bytes) -- see model.cu.
+void traffic_model(int64_t M, int64_t N, int64_t K, int64_t tm, int64_t tn, int64_t tk,
+                   int64_t in_bytes, int64_t acc_bytes, int64_t c_bytes, int64_t out[9]);
+
+// Predicted seconds of one product on a tensor-core variant (model.cu).
+double predict_seconds(int64_t M, int64_t N, int64_t K, int variant, int num_sms, int in_bytes,
+                       int out_bytes);
+
 // Output tile of a tensor-core variant (rows x columns).
 void tc_tile_shape(int variant, int* tile_m, int* tile_n);
 
