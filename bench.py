@@ -53,6 +53,10 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the benchmark line: time every tensor-core variant, the "
+                         "automatic choice and cuBLAS on a fixed list of BF16 shapes, one JSON "
+                         "line per shape")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the GEMM launches (no e2e, cuBLAS context or CPU "
                          "baseline); used for profiler captures")
@@ -416,8 +420,53 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+SWEEP_SHAPES = [(n, n, n) for n in (2048, 3072, 4096, 6144, 8192)] + [
+    (256, 8192, 4096), (8192, 256, 4096), (1024, 4096, 8192), (2048, 2048, 16384),
+    (12288, 12288, 2048), (1536, 1536, 1536), (2560, 2560, 2560), (5120, 5120, 1024)]
+
+
+def run_sweep():
+    """Median per-call TFLOP/s of each tensor-core variant, the automatic
+    choice and cuBLAS (torch.matmul) on BF16 inputs, BF16 output."""
+    import torch
+    import tiled_matrix_multiplication_output_gb300 as tg
+    tg.load_library(build_if_missing=True)
+    torch.cuda.set_device(0)
+
+    def timeit(f, steps):
+        for _ in range(5):
+            f()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record()
+        for i in range(steps):
+            f()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        return statistics.median([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
+
+    g = torch.Generator(device="cuda").manual_seed(0)
+    for M, N, K in SWEEP_SHAPES:
+        A = (torch.randn(M, K, device="cuda", generator=g) / math.sqrt(K)).bfloat16()
+        B = (torch.randn(K, N, device="cuda", generator=g) / math.sqrt(K)).bfloat16()
+        C = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        steps = max(20, min(300, int(2e12 / (2 * M * N * K))))
+        flops = 2.0 * M * N * K
+        row = {"shape": [M, N, K]}
+        for k in ("tc_128x128", "tc_128x256", "tc_256x256", "auto"):
+            ms = timeit(lambda: tg.matmul(A, B, out_dtype=torch.bfloat16, out=C, kernel=k), steps)
+            row[k] = round(flops / ms / 1e9, 1)
+        row["auto_pick"] = tg.KERNEL_NAMES[tg.gemm_select_kernel(
+            A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, tg.BF16, tg.F32, tg.BF16)]
+        row["cublas"] = round(flops / timeit(lambda: torch.matmul(A, B), steps) / 1e9, 1)
+        print(json.dumps(row), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep()
+        return
     world_env = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
