@@ -61,12 +61,12 @@ double predict_seconds(int64_t M, int64_t N, int64_t K, int variant, int num_sms
     const int units = (variant == TC_256x256) ? std::max(1, num_sms / 2) : std::max(1, num_sms);
     // Sustained dense rate per unit (CTA or CTA pair), in FLOP/s, as measured
     // for each tile shape on GB300.
-    const double per_sm = 11.0e12;  // ~1670 TFLOP/s over 152 SMs for the pair kernel
+    const double per_sm = 11.0e12;  // ~1680 TFLOP/s over 152 SMs for the pair kernel
     double eff = 1.0;
     if (variant == TC_128x256)
-        eff = 0.87;
+        eff = 0.84;
     else if (variant == TC_128x128)
-        eff = 0.60;
+        eff = 0.71;
     const double unit_rate = per_sm * eff * (variant == TC_256x256 ? 2.0 : 1.0);
     const int64_t tiles = ceil_div(M, tile_m) * ceil_div(N, tile_n);
     const int64_t waves = ceil_div(tiles, units);

@@ -65,13 +65,18 @@ constexpr int TC_THREADS = 192;  // 6 warps
 constexpr int TC_EPI_WARP0 = 2;
 constexpr int TC_STAGING_BYTES = 4096;  // 32 rows x 128 bytes per warp buffer
 
-template <int CG, int BN, int STAGES>
+// KSUB 64-wide K steps share one shared-memory stage (one barrier wait and
+// one commit per KSUB * 4 MMAs); sub-step j of a stage sits at j * SUB_A /
+// j * SUB_B.
+template <int CG, int BN, int STAGES, int KSUB = 1>
 struct TcLayout {
-    static constexpr int A_STAGE = TC_BM * TC_BK * 2;            // 16 KiB
+    static constexpr int SUB_A = TC_BM * TC_BK * 2;              // 16 KiB per K step
+    static constexpr int A_STAGE = KSUB * SUB_A;
     static constexpr int B_COLS = BN / CG;                       // B columns held per CTA
-    static constexpr int B_STAGE = TC_BK * B_COLS * 2;
+    static constexpr int SUB_B = TC_BK * B_COLS * 2;
+    static constexpr int B_STAGE = KSUB * SUB_B;
     static constexpr int B_BOXES = B_COLS / 64;                  // 64-column, 8 KiB boxes
-    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;        // bytes landing per CTA
+    static constexpr int SUB_BYTES = SUB_A + SUB_B;              // bytes per K step per CTA
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_STAGING = OFF_B + STAGES * B_STAGE;
@@ -302,13 +307,14 @@ __device__ __forceinline__ void tc_strip_to_smem(uint32_t taddr, uint32_t stagin
     }
 }
 
-template <int CG, int BN, int STAGES, typename OutT, bool A_MN, bool B_MN, bool SPLIT = false>
+template <int CG, int BN, int STAGES, typename OutT, bool A_MN, bool B_MN, bool SPLIT = false,
+          int KSUB = 1>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                    const TcParams p)
 {
-    using L = TcLayout<CG, BN, STAGES>;
+    using L = TcLayout<CG, BN, STAGES, KSUB>;
     constexpr int STRIP = TcOut<OutT>::STRIP;
     constexpr int TILE_M = TC_BM * CG;  // output rows per tile (per CTA pair)
 
@@ -378,17 +384,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const TcWork w = tc_work(t, p);
                 const int a_row = w.mb * TILE_M + static_cast<int>(rank) * TC_BM;
                 const int b_col = w.nb * BN + static_cast<int>(rank) * L::B_COLS;
-                for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += KSUB) {
+                    const int nsub = min(KSUB, w.kb_end - kb0);
                     if (!tc_wait(empty_bar(stage), phase ^ 1, watch)) {
                         ok = false;
                         break;
                     }
-                    if (kb != p.fault_skip_kblock) {  // test hook: -1 in normal use
+                    // test hook (-1 in normal use): skip the stage holding that K step
+                    if (p.fault_skip_kblock < kb0 || p.fault_skip_kblock >= kb0 + nsub) {
                         const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
                         if (leader)
-                            mbar_arrive_expect_tx(full_bar(stage), CG * L::STAGE_BYTES);
-                        const uint32_t dA = sA + stage * L::A_STAGE;
-                        const uint32_t dB = sB + stage * L::B_STAGE;
+                            mbar_arrive_expect_tx(full_bar(stage), CG * nsub * L::SUB_BYTES);
+#pragma unroll
+                        for (int sub = 0; sub < KSUB; ++sub) {
+                        if (sub >= nsub)
+                            break;
+                        const int kb = kb0 + sub;
+                        const uint32_t dA = sA + stage * L::A_STAGE + sub * L::SUB_A;
+                        const uint32_t dB = sB + stage * L::B_STAGE + sub * L::SUB_B;
                         auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
                             if constexpr (CG == 2)
                                 tma_load_2d_pair(dst, map, fb, x, y);
@@ -411,6 +424,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 load(dB + j * 8192, &tmB, b_col + 64 * j, kb * TC_BK);
                         } else {
                             load(dB, &tmB, kb * TC_BK, b_col);
+                        }
                         }
                         ++issued[stage];
                     }
@@ -453,14 +467,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+                for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += KSUB) {
+                    const int nsub = min(KSUB, w.kb_end - kb0);
                     if (!tc_wait(full_bar(stage), phase, watch)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = sA + stage * L::A_STAGE;
-                    const uint32_t b0 = sB + stage * L::B_STAGE;
+#pragma unroll
+                    for (int sub = 0; sub < KSUB; ++sub) {
+                    if (sub >= nsub)
+                        break;
+                    const uint32_t a0 = sA + stage * L::A_STAGE + sub * L::SUB_A;
+                    const uint32_t b0 = sB + stage * L::B_STAGE + sub * L::SUB_B;
 #pragma unroll
                     for (int k = 0; k < TC_BK / TC_UMMA_K; ++k) {
                         // K-major operand: rows of 128 bytes, 8-row groups 1024
@@ -472,7 +491,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                                     : smem_desc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bdesc = B_MN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
                                                     : smem_desc_sw128(b0 + k * 32, 16, 1024);
-                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, idesc, (kb != w.kb_begin) || k != 0);
+                        tc_mma_f16<CG>(d_tmem, adesc, bdesc, idesc,
+                                       (kb0 != w.kb_begin) || sub != 0 || k != 0);
+                    }
                     }
                     if constexpr (CG == 2)
                         tc_commit_pair(empty_bar(stage), 0x3);
