@@ -251,9 +251,15 @@ int gemm_select_kernel(const void* A, const void* B, const void* C, int64_t M, i
  * A_host (M x K), B_host (K x N) and C_host (M x N) are host buffers (pinned
  * memory gives asynchronous copies; pageable memory works but the copies
  * block).  dA, dB and dC are caller-owned device buffers of at least the same
- * sizes.  On `stream` the call enqueues the host-to-device copies of A and B,
- * the product, and the device-to-host copy of C; it returns after enqueueing
- * (synchronize the stream before reading C_host).  Errors as gemm_ex.
+ * sizes.  The call enqueues the host-to-device copies of A and B, the
+ * product, and the device-to-host copy of C, ordered after the work already
+ * on `stream` and before anything queued on it later; it returns after
+ * enqueueing (synchronize the stream before reading C_host).  Products of
+ * more than 1024 rows are pipelined in row panels: B is copied first, then
+ * the copy of one panel of A and the copy back of another panel of C
+ * overlap the product of a third, on two copy streams the library creates
+ * once per device (calls from several host threads are enqueued one at a
+ * time).  Errors as gemm_ex.
  */
 int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M, int64_t N,
                  int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,

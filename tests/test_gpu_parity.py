@@ -200,3 +200,30 @@ def test_stream_ordering_on_side_stream():
         Ch = C.cpu()
     s.synchronize()
     expect_close(Ch, A, B, with_output_rounding=False)
+
+
+def test_host_buffer_entry_point_pipelined():
+    """More than 1024 rows: the host-buffer path runs in row panels on its
+    own copy streams; the result is exact on integer inputs, and a second
+    call right after the first (other inputs, same device buffers) sees its
+    own inputs only."""
+    M, N, K = 4100, 520, 264            # 4 panels of 1280 rows, the last one ragged
+    s = torch.cuda.current_stream()
+    dA = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    dB = torch.empty(K, N, dtype=torch.bfloat16, device="cuda")
+    dC = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    outs = []
+    for seed in (15, 16):
+        A, B = inputs.draw(M, N, K, "bf16", "int", seed=seed)
+        Ah, Bh = A.pin_memory(), B.pin_memory()
+        C = torch.empty(M, N, dtype=torch.float32).pin_memory()
+        rc = tg.gemm_ex_host(Ah.data_ptr(), Bh.data_ptr(), C.data_ptr(), M, N, K, tg.BF16,
+                             tg.F32, tg.F32, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                             s.cuda_stream)
+        assert rc == 0
+        outs.append((A, B, C, Ah, Bh))
+    s.synchronize()
+    for A, B, C, _, _ in outs:
+        expect_exact(C, A, B)
+    # work queued after the call on the same stream sees the finished product
+    assert torch.equal(dC.cpu(), outs[-1][2])

@@ -388,6 +388,52 @@ extern "C" int gemm_ex_ws(const void* A, const void* B, void* C, int64_t M, int6
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+namespace tmmo {
+namespace {
+
+// Auxiliary streams and events of the pipelined host-buffer path, one set
+// per device, created on first use and kept until exit.
+constexpr int kMaxPanels = 8;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, b_done = nullptr, done = nullptr;
+    cudaEvent_t a_done[kMaxPanels] = {}, c_done[kMaxPanels] = {};
+    std::mutex mu;
+};
+HostPipe g_pipe[kMaxDevices];
+
+cudaError_t host_pipe(HostPipe** out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    HostPipe& h = g_pipe[dev];
+    std::lock_guard<std::mutex> g(h.mu);
+    if (!h.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if ((err = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (err = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (err = cudaEventCreateWithFlags(&h.start, ef)) != cudaSuccess ||
+            (err = cudaEventCreateWithFlags(&h.b_done, ef)) != cudaSuccess ||
+            (err = cudaEventCreateWithFlags(&h.done, ef)) != cudaSuccess)
+            return err;
+        for (int i = 0; i < kMaxPanels; ++i)
+            if ((err = cudaEventCreateWithFlags(&h.a_done[i], ef)) != cudaSuccess ||
+                (err = cudaEventCreateWithFlags(&h.c_done[i], ef)) != cudaSuccess)
+                return err;
+        h.ready = true;
+    }
+    *out = &h;
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace tmmo
+
 extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
                             int64_t N, int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
                             gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* stream)
@@ -403,18 +449,64 @@ extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t in_b = static_cast<size_t>(dt_size(in_dtype));
     const size_t out_b = static_cast<size_t>(dt_size(out_dtype));
-    if (K > 0) {
-        if (cudaMemcpyAsync(dA, A_host, size_t(M) * size_t(K) * in_b, cudaMemcpyHostToDevice, s) !=
-                cudaSuccess ||
-            cudaMemcpyAsync(dB, B_host, size_t(K) * size_t(N) * in_b, cudaMemcpyHostToDevice, s) !=
-                cudaSuccess)
+    const size_t a_row = size_t(K) * in_b, c_row = size_t(N) * out_b;
+    // Row panels of A and C: B is copied once, then the copy of A's panel
+    // i + 1 and of C's panel i - 1 overlap the product of panel i.  Panels
+    // are whole 256-row tile rows, at least 1024 rows; small products (or
+    // K == 0) run as one panel on the caller's stream.
+    int64_t panel = ((M + 3) / 4 + 255) / 256 * 256;
+    if (panel < 1024)
+        panel = 1024;
+    const int64_t panels = (M + panel - 1) / panel;
+    if (K == 0 || panels <= 1 || panels > kMaxPanels) {
+        if (K > 0) {
+            if (cudaMemcpyAsync(dA, A_host, size_t(M) * a_row, cudaMemcpyHostToDevice, s) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(dB, B_host, size_t(K) * size_t(N) * in_b, cudaMemcpyHostToDevice,
+                                s) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        }
+        rc = run(plain(dA, dB, dC, M, N, K, in_dtype, acc_dtype, out_dtype), GEMM_KERNEL_AUTO, s);
+        if (rc != GEMM_OK)
+            return rc;
+        if (cudaMemcpyAsync(C_host, dC, size_t(M) * c_row, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return GEMM_OK;
+    }
+    HostPipe* h = nullptr;
+    if (host_pipe(&h) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> g(h->mu);  // one pipelined call enqueues at a time per device
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // Everything starts after the work already queued on the caller's stream.
+    if (!ok(cudaEventRecord(h->start, s)) || !ok(cudaStreamWaitEvent(h->in, h->start, 0)) ||
+        !ok(cudaStreamWaitEvent(h->out, h->start, 0)))
+        return GEMM_ERR_CUDA;
+    if (!ok(cudaMemcpyAsync(dB, B_host, size_t(K) * size_t(N) * in_b, cudaMemcpyHostToDevice,
+                            h->in)) ||
+        !ok(cudaEventRecord(h->b_done, h->in)) || !ok(cudaStreamWaitEvent(s, h->b_done, 0)))
+        return GEMM_ERR_CUDA;
+    for (int64_t i = 0; i < panels; ++i) {
+        const int64_t r0 = i * panel;
+        const int64_t rows = (M - r0 < panel) ? M - r0 : panel;
+        const char* a_src = static_cast<const char*>(A_host) + size_t(r0) * a_row;
+        char* a_dst = static_cast<char*>(dA) + size_t(r0) * a_row;
+        char* c_dev = static_cast<char*>(dC) + size_t(r0) * c_row;
+        char* c_dst = static_cast<char*>(C_host) + size_t(r0) * c_row;
+        if (!ok(cudaMemcpyAsync(a_dst, a_src, size_t(rows) * a_row, cudaMemcpyHostToDevice, h->in)) ||
+            !ok(cudaEventRecord(h->a_done[i], h->in)) ||
+            !ok(cudaStreamWaitEvent(s, h->a_done[i], 0)))
+            return GEMM_ERR_CUDA;
+        rc = run(plain(a_dst, dB, c_dev, rows, N, K, in_dtype, acc_dtype, out_dtype),
+                 GEMM_KERNEL_AUTO, s);
+        if (rc != GEMM_OK)
+            return rc;
+        if (!ok(cudaEventRecord(h->c_done[i], s)) || !ok(cudaStreamWaitEvent(h->out, h->c_done[i], 0)) ||
+            !ok(cudaMemcpyAsync(c_dst, c_dev, size_t(rows) * c_row, cudaMemcpyDeviceToHost, h->out)))
             return GEMM_ERR_CUDA;
     }
-    rc = run(plain(dA, dB, dC, M, N, K, in_dtype, acc_dtype, out_dtype), GEMM_KERNEL_AUTO, s);
-    if (rc != GEMM_OK)
-        return rc;
-    if (cudaMemcpyAsync(C_host, dC, size_t(M) * size_t(N) * out_b, cudaMemcpyDeviceToHost, s) !=
-        cudaSuccess)
+    // The caller's stream resumes once the last panel of C is on the host.
+    if (!ok(cudaEventRecord(h->done, h->out)) || !ok(cudaStreamWaitEvent(s, h->done, 0)))
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
