@@ -178,13 +178,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` products of its own replica,
+    and the job took as long as the slowest rank (max_ms)."""
+    return flops_per_step * world * steps / (max_ms * 1e-3) / 1e12
 
 
 def cpu_oracle_rate(A, B, target_seconds: float):
@@ -330,7 +338,7 @@ def run_ours(args, rank, world, local):
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     flops = float(w.flops)
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_rate(flops, args.steps, world, total_ms)
 
     if args.kernel_only:
         if rank == 0:

@@ -94,3 +94,18 @@ def test_large_workload_sampled(name):
     # run-to-run determinism at full size
     C2 = run_gpu(A, B, _out(w), "auto")
     assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+
+
+def test_tall_product_many_tiles():
+    """M = 131072 rows (512 pair tiles, 1024 single-CTA tiles) with a short K:
+    sampled entries within the bound, row and column sums, on the automatic
+    choice and on gemm_ex_ws."""
+    A, B = inputs.draw(131072, 256, 136, "bf16", "normal", seed=30)
+    for C in (run_gpu(A, B, torch.bfloat16, "auto"),
+              tg.matmul_ws(A.cuda(), B.cuda(), out_dtype=torch.bfloat16).cpu()):
+        rows, cols = sample_indices(131072, 256, 4000, seed=31, tile_m=256, tile_n=256)
+        ref, ref_abs = oracle.gemm_entries(A, B, rows, cols)
+        got = C[torch.from_numpy(rows), torch.from_numpy(cols)].double().numpy()
+        half_ulp = HALF_ULP[torch.bfloat16] * np.abs(ref)
+        assert np.all(np.abs(got - ref) <= oracle.tolerance(ref_abs) + half_ulp)
+        _sums_check(C, A, B)
