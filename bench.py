@@ -57,6 +57,10 @@ def parse_args():
                     help="instead of the benchmark line: time every tensor-core variant, the "
                          "automatic choice and cuBLAS on a fixed list of BF16 shapes, one JSON "
                          "line per shape")
+    ap.add_argument("--rows", action="store_true",
+                    help="instead of the benchmark line: time the extended forms (transposed "
+                         "operands, alpha/beta, split-K, last-wave split) on fixed BF16 "
+                         "problems, one JSON line each")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the GEMM launches (no e2e, cuBLAS context or CPU "
                          "baseline); used for profiler captures")
@@ -470,10 +474,88 @@ def run_sweep():
         print(json.dumps(row), flush=True)
 
 
+def run_rows():
+    """Median per-call time and TFLOP/s of the extended entry points."""
+    import torch
+    import tiled_matrix_multiplication_output_gb300 as tg
+    tg.load_library(build_if_missing=True)
+    torch.cuda.set_device(0)
+
+    def timeit(f, steps):
+        for _ in range(5):
+            f()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record()
+        for i in range(steps):
+            f()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        return statistics.median([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
+
+    def emit(row, M, N, K, ms, **extra):
+        print(json.dumps({"row": row, "shape": [M, N, K], "us": round(ms * 1e3, 2),
+                          "tflops": round(2.0 * M * N * K / ms / 1e9, 1), **extra}), flush=True)
+
+    g = torch.Generator(device="cuda").manual_seed(0)
+    n = 8192
+    A0 = (torch.randn(n, n, device="cuda", generator=g) / math.sqrt(n)).bfloat16()
+    B0 = (torch.randn(n, n, device="cuda", generator=g) / math.sqrt(n)).bfloat16()
+    C = torch.empty(n, n, device="cuda", dtype=torch.bfloat16)
+    # f1: operand layouts on the pair kernel
+    for op_a, op_b in (("n", "n"), ("t", "n"), ("n", "t"), ("t", "t")):
+        A = A0.t().contiguous() if op_a == "t" else A0
+        B = B0.t().contiguous() if op_b == "t" else B0
+        ms = timeit(lambda: tg.addmm(A, B, C, op_a=op_a, op_b=op_b), 200)
+        emit("f1_layout_" + op_a + op_b, n, n, n, ms)
+    # f2: accumulate into C (reads C: 128 MiB more traffic per call)
+    ms = timeit(lambda: tg.addmm(A0, B0, C, alpha=1.0, beta=1.0), 200)
+    emit("f2_addmm_beta1", n, n, n, ms)
+    ms = timeit(lambda: tg.addmm(A0, B0, C, alpha=0.5, beta=0.0), 200)
+    emit("f2_alpha_only", n, n, n, ms)
+    del A0, B0, C
+    # f4: split-K on few-tile, long-K products; last-wave split on squares
+    for M, N, K in ((96, 200, 1000), (256, 256, 16384), (512, 512, 65536), (128, 1024, 8192)):
+        A = (torch.randn(M, K, device="cuda", generator=g) / math.sqrt(K)).bfloat16()
+        B = (torch.randn(K, N, device="cuda", generator=g) / math.sqrt(K)).bfloat16()
+        Cs = torch.empty(M, N, device="cuda")
+        ws = torch.empty(tg.gemm_splitk_workspace_size(M, N, K, 256) + 16, dtype=torch.uint8,
+                         device="cuda")
+        sh = torch.cuda.current_stream().cuda_stream
+        emit("f4_plain", M, N, K, timeit(lambda: tg.matmul(A, B, out=Cs), 200))
+        best = None
+        for splits in (2, 4, 8, 16, 32, 64):
+            ms = timeit(lambda: tg.gemm_splitk(A.data_ptr(), B.data_ptr(), Cs.data_ptr(), M, N, K,
+                                               splits, tg.BF16, tg.F32, tg.F32, ws.data_ptr(),
+                                               ws.numel(), sh), 200)
+            if best is None or ms < best[1]:
+                best = (splits, ms)
+        emit("f4_splitk_best", M, N, K, best[1], splits=best[0])
+    # whole waves vs the split last wave: interleaved rounds, so that heat and
+    # power-cap drift over the run does not favour whichever variant runs first
+    for m in (2560, 4096, 6144, 8192):
+        A = (torch.randn(m, m, device="cuda", generator=g) / math.sqrt(m)).bfloat16()
+        B = (torch.randn(m, m, device="cuda", generator=g) / math.sqrt(m)).bfloat16()
+        Cb = torch.empty(m, m, device="cuda", dtype=torch.bfloat16)
+        ws = torch.empty(tg.gemm_workspace_size(m, m, m), dtype=torch.uint8, device="cuda")
+        steps = 100 if m <= 4096 else 30
+        fns = {"f4_whole_waves": lambda: tg.matmul(A, B, out=Cb, out_dtype=torch.bfloat16),
+               "f4_last_wave_split": lambda: tg.matmul_ws(A, B, out=Cb, workspace=ws)}
+        rounds = {k: [] for k in fns}
+        for _ in range(6):
+            for k, f in fns.items():
+                rounds[k].append(timeit(f, steps))
+        for k in fns:
+            emit(k, m, m, m, statistics.median(rounds[k]))
+
+
 def main():
     args = parse_args()
     if args.sweep:
         run_sweep()
+        return
+    if args.rows:
+        run_rows()
         return
     world_env = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":

@@ -156,7 +156,9 @@ size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  * pair.  When the tile count is not a multiple of the pairs resident on the
  * GPU, the last wave leaves pairs idle; with a workspace, the tiles of that
  * last wave are instead split along K into as many pieces as there are idle
- * pairs, their FP32 partials go to `workspace` (caller-owned device memory,
+ * pairs (when that makes at least two pieces, each at least four 64-wide K
+ * steps long), their FP32 partials go to
+ * `workspace` (caller-owned device memory,
  * 16-byte aligned; gemm_workspace_size bytes always suffice), and a second
  * kernel on the same stream adds each tile's pieces in K order and writes
  * it.  The result differs from gemm_ex's only in the summation order of those

@@ -30,9 +30,10 @@ def _ws(A, B, out_dtype=torch.float32, workspace=None):
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_split_last_wave_exact_integers(out_dtype):
-    """2560 x 2560: 100 pair tiles over the resident pairs leaves a partial
-    last wave, which is split; ragged K (520 = 8 * 64 + 8)."""
-    A, B = inputs.draw(2560, 2560, 520, "bf16", "int", seed=90)
+    """2048 x 3072: 96 pair tiles over the resident pairs leaves a partial
+    last wave of 20 tiles, each split into 3 K ranges; ragged K
+    (776 = 12 * 64 + 8)."""
+    A, B = inputs.draw(2048, 3072, 776, "bf16", "int", seed=90)
     expect_exact(_ws(A, B, out_dtype), A, B)
 
 
