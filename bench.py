@@ -465,7 +465,7 @@ def run_sweep():
         steps = max(20, min(300, int(2e12 / (2 * M * N * K))))
         flops = 2.0 * M * N * K
         row = {"shape": [M, N, K]}
-        for k in ("tc_128x128", "tc_128x256", "tc_256x256", "auto"):
+        for k in ("tc_128x128", "tc_128x256", "tc_256x256", "tc_256x128", "auto"):
             ms = timeit(lambda: tg.matmul(A, B, out_dtype=torch.bfloat16, out=C, kernel=k), steps)
             row[k] = round(flops / ms / 1e9, 1)
         row["auto_pick"] = tg.KERNEL_NAMES[tg.gemm_select_kernel(

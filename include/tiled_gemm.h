@@ -69,7 +69,8 @@ typedef enum {
                                   element ("Tiled Matrix Multiplication", TPB = 3) */
     GEMM_KERNEL_TC_128x128 = 3,/* tcgen05, one CTA per 128 x 128 output tile */
     GEMM_KERNEL_TC_128x256 = 4,/* tcgen05, one CTA per 128 x 256 output tile */
-    GEMM_KERNEL_TC_256x256 = 5 /* tcgen05 cta_group::2, one CTA pair per 256 x 256 tile */
+    GEMM_KERNEL_TC_256x256 = 5,/* tcgen05 cta_group::2, one CTA pair per 256 x 256 tile */
+    GEMM_KERNEL_TC_256x128 = 6 /* tcgen05 cta_group::2, one CTA pair per 256 x 128 tile */
 } gemm_kernel_t;
 
 /*

@@ -41,7 +41,7 @@ def test_square_128_f16_and_traffic_model():
     w = inputs.WORKLOADS["square_128_f16"]
     A, B = inputs.make(w)
     C_ref, Cabs = oracle.gemm(A, B)
-    for kernel in ("auto", "tc_128x128", "tc_128x256", "tc_256x256", "simt"):
+    for kernel in ("auto", "tc_128x128", "tc_128x256", "tc_256x256", "tc_256x128", "simt"):
         tolerance_check(run_gpu(A, B, _out(w), kernel), C_ref, Cabs, with_output_rounding=False)
     g = load_golden("page_figures.txt")
     t = oracle.traffic(128, 128, 128, 16, 16, 32, in_bytes=2, acc_bytes=4, c_bytes=4)
@@ -53,7 +53,7 @@ def test_edge_96x200x1000_bf16_every_kernel():
     w = inputs.WORKLOADS["edge_96x200x1000_bf16"]
     A, B = inputs.make(w)
     C_ref, Cabs = oracle.gemm(A, B)
-    for kernel in ("auto", "tc_128x128", "tc_128x256", "tc_256x256", "simt", "simt_tpb3"):
+    for kernel in ("auto", "tc_128x128", "tc_128x256", "tc_256x256", "tc_256x128", "simt", "simt_tpb3"):
         tolerance_check(run_gpu(A, B, _out(w), kernel), C_ref, Cabs, with_output_rounding=False)
 
 

@@ -133,7 +133,7 @@ int auto_kernel(const Problem& q, int num_sms)
     const int in_b = dt_size(q.in_dtype), out_b = dt_size(q.out_dtype);
     int best = GEMM_KERNEL_TC_256x256;
     double best_t = predict_seconds(M, N, K, TC_256x256, num_sms, in_b, out_b);
-    for (int v : {GEMM_KERNEL_TC_128x256, GEMM_KERNEL_TC_128x128}) {
+    for (int v : {GEMM_KERNEL_TC_256x128, GEMM_KERNEL_TC_128x256, GEMM_KERNEL_TC_128x128}) {
         const double t = predict_seconds(M, N, K, v, num_sms, in_b, out_b);
         if (t < best_t * 0.98) {  // prefer the larger tile unless clearly slower
             best_t = t;
@@ -158,7 +158,7 @@ int run(const Problem& q, int kernel, cudaStream_t stream)
     int rc = validate_problem(q);
     if (rc != GEMM_OK)
         return rc;
-    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_TC_256x256)
+    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_TC_256x128)
         return GEMM_ERR_INVALID_VALUE;
     if (q.M == 0 || q.N == 0)
         return GEMM_OK;

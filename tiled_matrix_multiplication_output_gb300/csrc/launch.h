@@ -15,7 +15,10 @@ void note_launch();
 enum { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 
 // Tensor-core kernel variants; they match the gemm_kernel_t values.
-enum { TC_128x128 = 3, TC_128x256 = 4, TC_256x256 = 5 };
+enum { TC_128x128 = 3, TC_128x256 = 4, TC_256x256 = 5, TC_256x128 = 6 };
+
+// Whether a variant runs on CTA pairs (cta_group::2).
+inline bool tc_is_pair(int variant) { return variant == TC_256x256 || variant == TC_256x128; }
 
 struct SimtLaunch {
     bool tpb3;          // the 3 x 3 one-thread-per-output instance

@@ -45,7 +45,7 @@ void traffic_model(int64_t M, int64_t N, int64_t K, int64_t tm, int64_t tn, int6
 
 // Predicted seconds of one product on a tensor-core variant:
 //   compute: the tiles run in waves of `units` resident CTAs (pairs for the
-//     256 x 256 kernel); every wave costs one full tile of MMA work at the
+//     256 x 256 and 256 x 128 kernels); every wave costs one full tile of MMA work at the
 //     variant's measured tile throughput;
 //   feed: the traffic model's bytes (tile step tk = 64) at the measured
 //     on-chip (L2 -> SM) rate;
@@ -58,16 +58,18 @@ double predict_seconds(int64_t M, int64_t N, int64_t K, int variant, int num_sms
 {
     int tile_m, tile_n;
     tc_tile_shape(variant, &tile_m, &tile_n);
-    const int units = (variant == TC_256x256) ? std::max(1, num_sms / 2) : std::max(1, num_sms);
+    const int units = tc_is_pair(variant) ? std::max(1, num_sms / 2) : std::max(1, num_sms);
     // Sustained dense rate per unit (CTA or CTA pair), in FLOP/s, as measured
     // for each tile shape on GB300.
     const double per_sm = 11.0e12;  // ~1680 TFLOP/s over 152 SMs for the pair kernel
     double eff = 1.0;
-    if (variant == TC_128x256)
+    if (variant == TC_256x128)
+        eff = 0.68;
+    else if (variant == TC_128x256)
         eff = 0.84;
     else if (variant == TC_128x128)
-        eff = 0.71;
-    const double unit_rate = per_sm * eff * (variant == TC_256x256 ? 2.0 : 1.0);
+        eff = 0.67;
+    const double unit_rate = per_sm * eff * (tc_is_pair(variant) ? 2.0 : 1.0);
     const int64_t tiles = ceil_div(M, tile_m) * ceil_div(N, tile_n);
     const int64_t waves = ceil_div(tiles, units);
     const double tile_flops = 2.0 * tile_m * tile_n * static_cast<double>(K);

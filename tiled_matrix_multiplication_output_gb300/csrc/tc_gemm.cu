@@ -37,6 +37,10 @@ void tc_tile_shape(int variant, int* tile_m, int* tile_n)
         *tile_m = 128;
         *tile_n = 256;
         break;
+    case TC_256x128:
+        *tile_m = 256;
+        *tile_n = 128;
+        break;
     default:
         *tile_m = 256;
         *tile_n = 256;

@@ -29,6 +29,12 @@
 #ifndef TMMO_PAIR_KSUB
 #define TMMO_PAIR_KSUB 2     // 64-wide K steps per stage of the CTA-pair kernel
 #endif
+#ifndef TMMO_PAIR128_STAGES
+#define TMMO_PAIR128_STAGES 4  // stages of the 256 x 128 CTA-pair kernel
+#endif
+#ifndef TMMO_PAIR128_KSUB
+#define TMMO_PAIR128_KSUB 2
+#endif
 #ifndef TMMO_WIDE_STAGES
 #define TMMO_WIDE_STAGES 4   // stages of the 128 x 256 kernel
 #endif
@@ -262,6 +268,8 @@ cudaError_t launch_layout(const TcLaunch& l, cudaStream_t stream)
         return launch_out<1, 128, TMMO_SQ_STAGES, A_MN, B_MN, TMMO_SQ_KSUB>(l, stream);
     case TC_128x256:
         return launch_out<1, 256, TMMO_WIDE_STAGES, A_MN, B_MN, TMMO_WIDE_KSUB>(l, stream);
+    case TC_256x128:
+        return launch_out<2, 128, TMMO_PAIR128_STAGES, A_MN, B_MN, TMMO_PAIR128_KSUB>(l, stream);
     case TC_256x256:
         return launch_out<2, 256, TMMO_PAIR_STAGES, A_MN, B_MN, TMMO_PAIR_KSUB>(l, stream);
     default:
