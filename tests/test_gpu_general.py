@@ -102,3 +102,18 @@ def test_k0_general_is_beta_c():
 def test_bad_op_rejected():
     rc = tg.gemm_general(16, 16, 16, 4, 4, 4, 7, 0, 1.0, 0.0, tg.BF16, tg.F32, tg.F32, 0, None)
     assert rc == tg.binding.ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("op_a,op_b", OPS)
+@pytest.mark.parametrize("kernel", TC_KERNELS)
+@pytest.mark.parametrize("shape", [(304, 320, 192), (136, 192, 320), (520, 640, 1152)])
+def test_half_full_last_stage_exact(op_a, op_b, kernel, shape):
+    """K a multiple of 64 with an odd number of 64-wide K steps, so on the
+    kernels whose stages hold two K steps the last stage is half full; N a
+    multiple of 64 but not of the tile width; M ragged.  Integer inputs."""
+    M, N, K = shape
+    A0, B0 = inputs.draw(M, N, K, "f16", "int", seed=62)
+    A, B = _stored(A0, B0, op_a, op_b)
+    C = _run(A, B, op_a, op_b, kernel)
+    ref, _ = oracle.gemm_general(A, B, op_a, op_b)
+    np.testing.assert_array_equal(C.double().numpy(), oracle.round_to(ref, torch.float32).double().numpy())

@@ -178,6 +178,20 @@ __device__ __forceinline__ void bulk_wait_group_all()
 
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (TMA store, tcgen05).
+// Programmatic dependent launch.  launch_dependents lets a grid launched
+// after this one with programmatic stream serialization start its blocks
+// once every block of this grid has issued it (or exited); wait, in that
+// dependent grid, blocks until the grids it depends on have completed and
+// their memory operations are visible.  Both are no-ops without such a launch.
+__device__ __forceinline__ void grid_dep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

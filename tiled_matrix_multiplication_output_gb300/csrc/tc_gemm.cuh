@@ -338,6 +338,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int unit = (CG == 2) ? (blockIdx.x >> 1) : blockIdx.x;   // CTA or CTA pair index
     const int num_units = (CG == 2) ? (gridDim.x >> 1) : gridDim.x;
     const TcWatch watch{abort_flag, p.status, p.wait_budget};
+    // A reduction launched after this kernel (split partials) may place its
+    // blocks now; they wait for this grid to complete before reading.
+    grid_dep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {

@@ -52,37 +52,73 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* src)
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// Launches a reduction kernel as a programmatic dependent of the tensor-core
+// kernel before it on the stream: its blocks may be placed while that kernel
+// still runs (it signals launch_dependents at its start) and start reading
+// as soon as it completes, without a launch gap.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, cudaStream_t stream,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    note_launch();
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, static_cast<Params>(args)...);
+    if (err != cudaSuccess)
+        return err;
+    return cudaGetLastError();
+}
+
+// out = alpha * acc + beta * C_old, four elements.
+template <typename OutT>
+__device__ __forceinline__ void finish4(OutT* dst, float4 acc, float alpha, float beta)
+{
+    acc.x *= alpha;
+    acc.y *= alpha;
+    acc.z *= alpha;
+    acc.w *= alpha;
+    if (beta != 0.0f) {
+        const float4 c = load4(dst);
+        acc.x = fmaf(beta, c.x, acc.x);
+        acc.y = fmaf(beta, c.y, acc.y);
+        acc.z = fmaf(beta, c.z, acc.z);
+        acc.w = fmaf(beta, c.w, acc.w);
+    }
+    store4(dst, acc);
+}
+
+__device__ __forceinline__ void add4(float4& a, const float4 b)
+{
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+
 // C[i] = alpha * sum_s ws[s][i] + beta * C[i], four elements per step
 // (M * N is a multiple of 4 because N is).
 template <typename OutT>
 __global__ void __launch_bounds__(256)
-    splitk_reduce_kernel(const float* __restrict__ ws, OutT* C, long long mn, int splits,
-                         float alpha, float beta)
+    splitk_reduce_kernel(const float* __restrict__ ws, OutT* __restrict__ C, long long mn,
+                         int splits, float alpha, float beta)
 {
+    grid_dep_wait();
     const long long n4 = mn / 4;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += stride) {
         float4 acc = load4(ws + 4 * i);
-        for (int s = 1; s < splits; ++s) {
-            const float4 v = load4(ws + static_cast<long long>(s) * mn + 4 * i);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        acc.x *= alpha;
-        acc.y *= alpha;
-        acc.z *= alpha;
-        acc.w *= alpha;
-        if (beta != 0.0f) {
-            const float4 c = load4(C + 4 * i);
-            acc.x = fmaf(beta, c.x, acc.x);
-            acc.y = fmaf(beta, c.y, acc.y);
-            acc.z = fmaf(beta, c.z, acc.z);
-            acc.w = fmaf(beta, c.w, acc.w);
-        }
-        store4(C + 4 * i, acc);
+        for (int s = 1; s < splits; ++s)
+            add4(acc, load4(ws + static_cast<long long>(s) * mn + 4 * i));
+        finish4(C + 4 * i, acc, alpha, beta);
     }
 }
 
@@ -93,57 +129,63 @@ cudaError_t launch_reduce(const TcLaunch& l, int splits, cudaStream_t stream)
     const long long n4 = mn / 4;
     const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 8;
     const int grid = static_cast<int>(std::max<long long>(1, std::min((n4 + 255) / 256, cap)));
-    note_launch();
-    splitk_reduce_kernel<OutT><<<grid, 256, 0, stream>>>(l.workspace, static_cast<OutT*>(l.C), mn,
-                                                        splits, l.alpha, l.beta);
-    return cudaGetLastError();
+    return launch_dependent(splitk_reduce_kernel<OutT>, dim3(grid), dim3(256), stream,
+                            l.workspace, static_cast<OutT*>(l.C), mn, splits, l.alpha, l.beta);
 }
 
 // Tail reduction of the hybrid plan: block (x = tail tile, y = band of 16
 // rows) sums the `splits` FP32 partials of its tile rows in split order and
-// writes the part of C inside M x N, four columns per thread and step.
-template <typename OutT>
-__global__ void __launch_bounds__(256)
-    tail_reduce_kernel(const float* __restrict__ ws, OutT* C, TcParams p, int tile_m, int tile_n,
-                       int splits)
+// writes the part of C inside M x N.  Each thread owns TAIL_ITEMS groups of
+// four columns and issues the loads of all of them before adding, so that
+// many loads are in flight per thread.
+constexpr int TAIL_BAND_ROWS = 16;
+constexpr int TAIL_THREADS = 256;
+
+template <typename OutT, int ITEMS>
+__global__ void __launch_bounds__(TAIL_THREADS)
+    tail_reduce_kernel(const float* __restrict__ ws, OutT* __restrict__ C, TcParams p, int tile_m,
+                       int tile_n, int splits)
 {
+    grid_dep_wait();
     const int tail = blockIdx.x;
     int mb, nb;
     tc_tile_coords(p.dp_tiles + tail, p, mb, nb);
     const long long tile_elems = static_cast<long long>(tile_m) * tile_n;
     const float* base = ws + static_cast<long long>(tail) * splits * tile_elems;
     const int groups_per_row = tile_n / 4;
-    const int band_rows = 16;
-    for (int g = threadIdx.x; g < band_rows * groups_per_row; g += blockDim.x) {
-        const int r = blockIdx.y * band_rows + g / groups_per_row;
+    long long off[ITEMS];
+    long long dst[ITEMS];
+    bool live[ITEMS];
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        const int g = threadIdx.x + i * TAIL_THREADS;
+        const int r = blockIdx.y * TAIL_BAND_ROWS + g / groups_per_row;
         const int c = (g % groups_per_row) * 4;
         const int grow = mb * tile_m + r;
         const int gcol = nb * tile_n + c;
-        if (r >= tile_m || grow >= p.M || gcol >= p.N)
-            continue;  // N is a multiple of 4, so a group lies wholly inside or outside
-        const long long off = static_cast<long long>(r) * tile_n + c;
-        float4 acc = load4(base + off);
-        for (int s = 1; s < splits; ++s) {
-            const float4 v = load4(base + static_cast<long long>(s) * tile_elems + off);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        acc.x *= p.alpha;
-        acc.y *= p.alpha;
-        acc.z *= p.alpha;
-        acc.w *= p.alpha;
-        OutT* dst = C + static_cast<long long>(grow) * p.N + gcol;
-        if (p.beta != 0.0f) {
-            const float4 cv = load4(dst);
-            acc.x = fmaf(p.beta, cv.x, acc.x);
-            acc.y = fmaf(p.beta, cv.y, acc.y);
-            acc.z = fmaf(p.beta, cv.z, acc.z);
-            acc.w = fmaf(p.beta, cv.w, acc.w);
-        }
-        store4(dst, acc);
+        // N is a multiple of 4, so a group lies wholly inside or outside C
+        live[i] = g < TAIL_BAND_ROWS * groups_per_row && r < tile_m && grow < p.M && gcol < p.N;
+        off[i] = static_cast<long long>(r) * tile_n + c;
+        dst[i] = static_cast<long long>(grow) * p.N + gcol;
     }
+    float4 acc[ITEMS];
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i)
+        acc[i] = live[i] ? load4(base + off[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 1; s < splits; ++s) {
+        const float* part = base + static_cast<long long>(s) * tile_elems;
+        float4 v[ITEMS];
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i)
+            v[i] = live[i] ? load4(part + off[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i)
+            add4(acc[i], v[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i)
+        if (live[i])
+            finish4(C + dst[i], acc[i], p.alpha, p.beta);
 }
 
 template <typename OutT>
@@ -159,11 +201,17 @@ cudaError_t launch_tail(const TcLaunch& l, const int* plan, cudaStream_t stream)
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.alpha = l.alpha;
     p.beta = l.beta;
-    const dim3 grid(plan[2], (plan[6] + 15) / 16, 1);
-    note_launch();
-    tail_reduce_kernel<OutT><<<grid, 256, 0, stream>>>(l.workspace, static_cast<OutT*>(l.C), p,
-                                                       plan[6], plan[7], plan[1]);
-    return cudaGetLastError();
+    const int tile_m = plan[6], tile_n = plan[7];
+    const dim3 grid(plan[2], (tile_m + TAIL_BAND_ROWS - 1) / TAIL_BAND_ROWS, 1);
+    // groups of four columns per band, spread over the block's threads
+    const int items = (TAIL_BAND_ROWS * (tile_n / 4) + TAIL_THREADS - 1) / TAIL_THREADS;
+    if (items <= 2)
+        return launch_dependent(tail_reduce_kernel<OutT, 2>, grid, dim3(TAIL_THREADS), stream,
+                                l.workspace, static_cast<OutT*>(l.C), p, tile_m, tile_n, plan[1]);
+    if (items <= 4)
+        return launch_dependent(tail_reduce_kernel<OutT, 4>, grid, dim3(TAIL_THREADS), stream,
+                                l.workspace, static_cast<OutT*>(l.C), p, tile_m, tile_n, plan[1]);
+    return cudaErrorInvalidValue;  // tiles are at most 256 columns wide
 }
 
 }  // namespace
