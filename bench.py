@@ -3,7 +3,8 @@
 One step is one C = A @ B of the chosen workload (default: 8192^3, BF16
 inputs N(0,1)/sqrt(K), FP32 accumulation, BF16 output) through the C ABI,
 with A and B resident in HBM.  A + B + C take 384 MiB, more than the 129 MB
-L2, so consecutive steps cannot reuse inputs from L2.
+L2, so consecutive steps cannot reuse inputs from L2.  Smaller workloads
+(--workload) overwrite L2 between steps, outside each step's own events.
 
 Prints ONE JSON line (rank 0).  Keys beyond the common ones:
   roofline      dominant kernel vs the measured dense BF16 tensor peak
@@ -262,12 +263,55 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+L2_BYTES = 129e6   # GB300 L2 capacity
+
+
+def footprint_bytes(w):
+    in_b = 4 if w.in_dtype == "f32" else 2
+    out_b = 4 if w.out_dtype == "f32" else 2
+    return (w.M * w.K + w.K * w.N) * in_b + w.M * w.N * out_b
+
+
+def needs_flush(w) -> bool:
+    """Whether A, B and C together fit in L2, so that consecutive steps would
+    find their inputs there: such workloads flush L2 between steps."""
+    return footprint_bytes(w) <= L2_BYTES
+
+
 def config_of(w, kernel):
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in_dtype": w.in_dtype,
             "acc_dtype": "f32", "out_dtype": w.out_dtype, "layout": "row-major A, B, C",
             "kernel": kernel, "dist": w.dist, "seed": w.seed,
-            "l2": "A+B+C larger than L2" if (w.M * w.K + w.K * w.N) * 2 + w.M * w.N * 2 > 129e6
-            else "inputs smaller than L2 (small workload)"}
+            "l2": ("L2 flushed between steps (a 2 x L2 write outside each step's events); "
+                   "time = sum of per-step event times") if needs_flush(w)
+            else "A+B+C larger than L2"}
+
+
+def timed_loop(fn, steps, stream, flush_buf):
+    """Runs fn `steps` times on `stream` and returns (total_ms, per-step ms).
+    Without a flush buffer the steps run back to back between two events
+    (per-step events in between); with one, every step has its own pair of
+    events and L2 is overwritten between steps, outside them."""
+    import torch
+    if flush_buf is None:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
+            fn()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(stream.device)
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+        return ev[0].elapsed_time(ev[-1]), per
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        es[i].record(stream)
+        fn()
+        ee[i].record(stream)
+        flush_buf.zero_()
+    torch.cuda.synchronize(stream.device)
+    per = [es[i].elapsed_time(ee[i]) for i in range(steps)]
+    return sum(per), per
 
 
 def run_ours(args, rank, world, local):
@@ -318,7 +362,8 @@ def run_ours(args, rank, world, local):
         raise tg.GemmError(rc, "warm-up")
 
     # ---- timed region: K steps, events around every launch
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    flush_buf = (torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev)
+                 if needs_flush(w) else None)
     sampler = ClockSampler(local) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -326,16 +371,10 @@ def run_ours(args, rank, world, local):
         sampler.start()
         time.sleep(0.25)
     launches0 = tg.gemm_launch_count()
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize(dev)
+    total_ms, per_launch = timed_loop(step, args.steps, stream, flush_buf)
     launches = tg.gemm_launch_count() - launches0
     barrier(world)
     clocks = sampler.stop() if sampler else None
-    total_ms = ev[0].elapsed_time(ev[-1])
-    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     rc = tg.gemm_device_status(sh)
     if rc != 0:
         raise tg.GemmError(rc, "timed region")
@@ -384,15 +423,9 @@ def run_ours(args, rank, world, local):
     # ---- cuBLAS on the same inputs, as context only
     for _ in range(5):
         torch.matmul(A, B)
-    c0 = torch.cuda.Event(enable_timing=True)
-    c1 = torch.cuda.Event(enable_timing=True)
     n_cublas = args.steps   # same length as our timed loop, so both run at sustained clocks
-    c0.record(stream)
-    for _ in range(n_cublas):
-        torch.matmul(A, B)
-    c1.record(stream)
-    torch.cuda.synchronize(dev)
-    cublas_tflops = flops * n_cublas / (c0.elapsed_time(c1) * 1e-3) / 1e12
+    cublas_ms, _ = timed_loop(lambda: torch.matmul(A, B), n_cublas, stream, flush_buf)
+    cublas_tflops = flops * n_cublas / (cublas_ms * 1e-3) / 1e12
 
     if rank != 0:
         return
