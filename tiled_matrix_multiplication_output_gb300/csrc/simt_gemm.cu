@@ -22,6 +22,9 @@
 //    round-to-nearest-even;
 //  * the grid is 1-D and each block strides over output tiles, so any M, N
 //    fit the launch limits;
+//  * the next K tile is fetched into registers while the current one is
+//    multiplied from shared memory, so global latency is paid once per tile
+//    and overlapped with the FMAs;
 //  * transposed operands (A stored K x M, B stored N x K) are read through
 //    strides, with the staging loop walking the contiguous dimension so
 //    global reads stay coalesced; the store computes alpha * acc + beta * C
@@ -58,6 +61,8 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
     constexpr int TX = BN / TN;  // threads along N
     constexpr int TY = BM / TM;  // threads along M
     constexpr int NT = TX * TY;
+    constexpr int LA = (BM * BK + NT - 1) / NT;  // A elements each thread stages per K tile
+    constexpr int LB = (BK * BN + NT - 1) / NT;  // B elements each thread stages per K tile
     __shared__ float As[BK][BM + 1];
     __shared__ float Bs[BK][BN + 1];
 
@@ -67,6 +72,50 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
     const int tiles_n = (N + BN - 1) / BN;
     const int tiles_m = (M + BM - 1) / BM;
     const long long num_tiles = static_cast<long long>(tiles_m) * tiles_n;
+
+    // The next K tile is read from global memory into registers (all of a
+    // thread's loads in flight together) while the current one is used from
+    // shared memory; it is stored after the barrier that ends that use.
+    float ra[LA], rb[LB];
+    auto load_tile = [&](int m0, int n0, int k0) {
+        // A tile (BM x BK): consecutive threads walk the dimension that is
+        // contiguous in memory (k for A as stored, m for A transposed).
+#pragma unroll
+        for (int r = 0; r < LA; ++r) {
+            const int e = tid + r * NT;
+            const int i = op_a ? e % BM : e / BK;
+            const int k = op_a ? e / BM : e % BK;
+            const int gm = m0 + i, gk = k0 + k;
+            const long long off = op_a ? static_cast<long long>(gk) * M + gm
+                                       : static_cast<long long>(gm) * K + gk;
+            ra[r] = (e < BM * BK && gm < M && gk < K) ? to_f32(A[off]) : 0.0f;
+        }
+        // B tile (BK x BN): n contiguous for B as stored, k for B transposed.
+#pragma unroll
+        for (int r = 0; r < LB; ++r) {
+            const int e = tid + r * NT;
+            const int k = op_b ? e % BK : e / BN;
+            const int j = op_b ? e / BK : e % BN;
+            const int gk = k0 + k, gn = n0 + j;
+            const long long off = op_b ? static_cast<long long>(gn) * K + gk
+                                       : static_cast<long long>(gk) * N + gn;
+            rb[r] = (e < BK * BN && gk < K && gn < N) ? to_f32(B[off]) : 0.0f;
+        }
+    };
+    auto store_tile = [&]() {
+#pragma unroll
+        for (int r = 0; r < LA; ++r) {
+            const int e = tid + r * NT;
+            if (e < BM * BK)
+                As[op_a ? e / BM : e % BK][op_a ? e % BM : e / BK] = ra[r];
+        }
+#pragma unroll
+        for (int r = 0; r < LB; ++r) {
+            const int e = tid + r * NT;
+            if (e < BK * BN)
+                Bs[op_b ? e % BK : e / BN][op_b ? e / BK : e % BN] = rb[r];
+        }
+    };
 
     for (long long tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         const int m0 = static_cast<int>(tile / tiles_n) * BM;
@@ -79,29 +128,15 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
             for (int j = 0; j < TN; ++j)
                 acc[i][j] = 0.0f;
 
-        for (int k0 = 0; k0 < K; k0 += BK) {
-            // Stage the A tile (BM x BK), stored K-major; consecutive
-            // threads walk the dimension that is contiguous in memory (k for
-            // A as stored, m for A transposed), so global reads coalesce.
-            for (int e = tid; e < BM * BK; e += NT) {
-                const int i = op_a ? e % BM : e / BK;
-                const int k = op_a ? e / BM : e % BK;
-                const int gm = m0 + i, gk = k0 + k;
-                const long long off = op_a ? static_cast<long long>(gk) * M + gm
-                                           : static_cast<long long>(gm) * K + gk;
-                As[k][i] = (gm < M && gk < K) ? to_f32(A[off]) : 0.0f;
-            }
-            // Stage the B tile (BK x BN): n contiguous for B as stored, k for
-            // B transposed.
-            for (int e = tid; e < BK * BN; e += NT) {
-                const int k = op_b ? e % BK : e / BN;
-                const int j = op_b ? e / BK : e % BN;
-                const int gk = k0 + k, gn = n0 + j;
-                const long long off = op_b ? static_cast<long long>(gn) * K + gk
-                                           : static_cast<long long>(gk) * N + gn;
-                Bs[k][j] = (gk < K && gn < N) ? to_f32(B[off]) : 0.0f;
-            }
+        if (K > 0) {
+            load_tile(m0, n0, 0);
+            store_tile();
             __syncthreads();
+        }
+        for (int k0 = 0; k0 < K; k0 += BK) {
+            const bool more = k0 + BK < K;
+            if (more)
+                load_tile(m0, n0, k0 + BK);
 #pragma unroll
             for (int k = 0; k < BK; ++k) {
                 float a[TM], b[TN];
@@ -118,6 +153,10 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
                         acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
             }
             __syncthreads();
+            if (more) {
+                store_tile();
+                __syncthreads();
+            }
         }
 
 #pragma unroll
