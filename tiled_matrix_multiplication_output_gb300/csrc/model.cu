@@ -78,7 +78,10 @@ double predict_seconds(int64_t M, int64_t N, int64_t K, int variant, int num_sms
     traffic_model(M, N, K, tile_m, tile_n, 64, in_bytes, 4, out_bytes, t);
     const double l2_rate = 14.0e12;  // bytes/s delivered from L2 to the SMs, measured
     const double t_feed = static_cast<double>(t[3]) / l2_rate;
-    const double t_launch = 4.0e-6;
+    // Fixed cost of a launch: a CTA-pair kernel also sets up its clusters and
+    // synchronizes both CTAs around TMEM, measured about 2 us more than the
+    // single-CTA kernel on one-tile problems (128^3 .. 1024^3 BF16).
+    const double t_launch = tc_is_pair(variant) ? 6.0e-6 : 4.0e-6;
     return std::max(t_compute, t_feed) + t_launch;
 }
 
