@@ -343,11 +343,15 @@ def run_ours(args, rank, world, local):
     sh = stream.cuda_stream
     # The automatic path goes through gemm_ex_ws with a workspace allocated
     # here, before any timing: on the CTA-pair kernel it splits the tiles of
-    # the last, partial wave along K (a second, small launch sums them).
+    # the last, partial wave along K, and products with few tiles and a long
+    # K are split along K throughout (a second, small launch sums the pieces).
     use_ws = kid == 0
     ws_bytes = tg.gemm_workspace_size(w.M, w.N, w.K) if use_ws else 0
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    if use_ws and chosen == tg.KERNELS["tc_256x256"]:
+    ws_splits = tg.gemm_ws_split_count(w.M, w.N, w.K, in_code, tg.F32, out_code) if use_ws else 0
+    if ws_splits > 0:
+        kname = f"tc_128x128+split_k{ws_splits}"
+    elif use_ws and chosen == tg.KERNELS["tc_256x256"]:
         kname = "tc_256x256+split_last_wave"
 
     def step():

@@ -145,8 +145,9 @@ int gemm_general(const void* A, const void* B, void* C, int64_t M, int64_t N, in
 
 /*
  * gemm_workspace_size -- bytes of workspace gemm_ex_ws can use for these
- * sizes on the current device (an upper bound: one 256 x 256 FP32 tile per
- * pair of SMs), or 0 for empty products or when no device is available.
+ * sizes on the current device: one 256 x 256 FP32 tile per pair of SMs, or,
+ * for the few-tile products it splits along K, their split partials when
+ * those are larger.  0 for empty products or when no device is available.
  */
 size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -168,10 +169,29 @@ size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  * kernel, this is gemm_ex.  Calls sharing a workspace must not overlap in
  * time.  Errors as gemm_ex, plus GEMM_ERR_INVALID_VALUE for a misaligned
  * workspace.
+ *
+ * Products with few output tiles and a long K take the other form of the
+ * same idea (see gemm_ws_split_count): every tile is split along K, as
+ * gemm_splitk does, so that the otherwise idle SMs share the K loop.
  */
 int gemm_ex_ws(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,
                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gemm_ws_split_count -- for products with few output tiles, the number of
+ * K ranges gemm_ex_ws splits them into (as gemm_splitk with that many
+ * splits), or 0 when it does not.  The rule: a tensor-core product whose
+ * 128 x 128 output tiles occupy at most a quarter of the SMs, with K of at
+ * least 512, is split so that up to one unit of work runs per SM, into at
+ * most 16 ranges.  gemm_ex_ws does so only when its workspace holds
+ * gemm_splitk_workspace_size(M, N, K, count) bytes, which
+ * gemm_workspace_size always covers.  There is no counterpart in the pages:
+ * they accumulate each tile over all of K in one place.  Returns the count,
+ * 0, or a negated gemm_status_t (bad sizes or types, no device).
+ */
+int gemm_ws_split_count(int64_t M, int64_t N, int64_t K, gemm_dtype_t in_dtype,
+                        gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype);
 
 /*
  * gemm_splitk_workspace_size -- bytes of FP32 workspace gemm_splitk needs:

@@ -74,3 +74,39 @@ def test_splitk_unaligned_falls_back_exactly():
     A, B = inputs.draw(50, 37, 333, "f16", "int", seed=72)   # no TMA-legal pitches
     C = tg.matmul_splitk(A.cuda(), B.cuda(), 4)
     expect_exact(C.cpu(), A, B)
+
+
+def test_gemm_ex_ws_splits_few_tile_products():
+    """gemm_ex_ws takes split-K for few output tiles and a long K (the
+    96 x 200 x 1000 workload's shape): same partial order as gemm_splitk
+    with the reported count, exact on integer inputs, two launches; large
+    products and short K are not split."""
+    M, N, K = 96, 200, 1000
+    count = tg.gemm_ws_split_count(M, N, K, tg.BF16, tg.F32, tg.F32)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert count == min(sms // 2, 16)     # 2 tiles, 16 K steps: up to one unit per SM
+    assert tg.gemm_ws_split_count(8192, 8192, 8192, tg.BF16, tg.F32, tg.BF16) == 0
+    assert tg.gemm_ws_split_count(128, 128, 128, tg.F16, tg.F32, tg.F32) == 0
+    assert tg.gemm_ws_split_count(96, 200, 1000, tg.F32, tg.F32, tg.F32) == 0   # SIMT path
+    assert tg.gemm_ws_split_count(-1, 200, 1000, tg.BF16, tg.F32, tg.F32) == -tg.binding.ERR_INVALID_VALUE
+    A, B = inputs.draw(M, N, K, "bf16", "int", seed=31)
+    dA, dB = A.cuda(), B.cuda()
+    s = torch.cuda.current_stream().cuda_stream
+    ws_bytes = tg.gemm_workspace_size(M, N, K)
+    assert ws_bytes >= tg.gemm_splitk_workspace_size(M, N, K, count)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    C = torch.full((M, N), float("nan"), device="cuda")
+    n0 = tg.gemm_launch_count()
+    rc = tg.gemm_ex_ws(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, tg.BF16, tg.F32,
+                       tg.F32, ws.data_ptr(), ws_bytes, s)
+    assert rc == 0
+    assert tg.gemm_launch_count() - n0 == 2
+    assert tg.gemm_device_status(s) == 0
+    expect_exact(C.cpu(), A, B)
+    ws2 = torch.empty(tg.gemm_splitk_workspace_size(M, N, K, count), dtype=torch.uint8, device="cuda")
+    C2 = torch.empty((M, N), device="cuda")
+    rc = tg.gemm_splitk(dA.data_ptr(), dB.data_ptr(), C2.data_ptr(), M, N, K, count, tg.BF16,
+                        tg.F32, tg.F32, ws2.data_ptr(), ws2.numel(), s)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert torch.equal(C, C2)

@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     gemm_device_status, gemm_error_string, gemm_ex, gemm_ex_host, gemm_ex_kernel, gemm_ex_ws,
     gemm_general, gemm_launch_count, gemm_traffic_model, gemm_workspace_size, matmul_ws,
     gemm_select_kernel, gemm_splitk, gemm_splitk_noalloc, gemm_splitk_workspace_size,
+    gemm_ws_split_count,
     header_functions, library_path,
     load_library, matmul, matmul_splitk,
 )

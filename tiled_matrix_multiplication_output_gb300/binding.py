@@ -48,6 +48,7 @@ _SIGNATURES = {
     "gemm_ex": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p], _int),
     "gemm_ex_kernel": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _int, _p], _int),
     "gemm_select_kernel": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int], _int),
+    "gemm_ws_split_count": ([_i64, _i64, _i64, _int, _int, _int], _int),
     "gemm_general": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, ctypes.c_float, ctypes.c_float,
                       _int, _int, _int, _int, _p], _int),
     "gemm_ex_host": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, _p, _p, _p], _int),
@@ -136,6 +137,10 @@ def gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype
 
 def gemm_workspace_size(M, N, K) -> int:
     return load_library().gemm_workspace_size(M, N, K)
+
+
+def gemm_ws_split_count(M, N, K, in_dtype, acc_dtype, out_dtype) -> int:
+    return load_library().gemm_ws_split_count(M, N, K, in_dtype, acc_dtype, out_dtype)
 
 
 def gemm_ex_ws(A, B, C, M, N, K, in_dtype, acc_dtype, out_dtype, workspace, workspace_bytes,

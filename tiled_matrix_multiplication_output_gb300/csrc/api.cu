@@ -332,6 +332,28 @@ extern "C" int gemm_splitk(const void* A, const void* B, void* C, int64_t M, int
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+namespace tmmo {
+namespace {
+
+// K ranges gemm_ex_ws splits a product with few output tiles into: when the
+// 128 x 128 tiles would occupy at most a quarter of the SMs and K holds at
+// least eight 64-wide steps, K is divided so that up to one unit of work runs
+// per SM, at most 16 ranges.  0 = no split.
+int few_tile_splits(int64_t M, int64_t N, int64_t K, int num_sms)
+{
+    const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+    const int64_t k_blocks = (K + 63) / 64;
+    if (tiles <= 0 || tiles * 4 > num_sms || k_blocks < 8)
+        return 0;
+    const int64_t s = std::min<int64_t>(std::min<int64_t>(num_sms / tiles, k_blocks), 16);
+    if (s < 2)
+        return 0;
+    return splitk_used_splits(K, static_cast<int>(s));
+}
+
+}  // namespace
+}  // namespace tmmo
+
 extern "C" size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 0 || N <= 0 || K <= 0)
@@ -339,8 +361,32 @@ extern "C" size_t gemm_workspace_size(int64_t M, int64_t N, int64_t K)
     DeviceInfo d;
     if (device_info(&d) != cudaSuccess)
         return 0;
-    // At most one split piece per resident CTA pair, each a 256 x 256 FP32 tile.
-    return static_cast<size_t>(d.num_sms / 2) * 256u * 256u * 4u;
+    // Last-wave split: at most one piece per resident CTA pair, each a
+    // 256 x 256 FP32 tile.  Few-tile split-K: its [splits][M][N] partials.
+    const size_t tail = static_cast<size_t>(d.num_sms / 2) * 256u * 256u * 4u;
+    const int s = few_tile_splits(M, N, K, d.num_sms);
+    const size_t split = s > 1 ? gemm_splitk_workspace_size(M, N, K, s) : 0;
+    return std::max(tail, split);
+}
+
+extern "C" int gemm_ws_split_count(int64_t M, int64_t N, int64_t K, gemm_dtype_t in_dtype,
+                                   gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype)
+{
+    // Operand addresses do not enter the decision beyond 16-byte alignment,
+    // so any aligned non-null address stands in for them here.
+    const void* any = reinterpret_cast<const void*>(uintptr_t(256));
+    const int rc = validate(any, any, any, M, N, K, in_dtype, acc_dtype, out_dtype);
+    if (rc != GEMM_OK)
+        return -rc;
+    Problem q = plain(any, any, const_cast<void*>(any), M, N, K, in_dtype, acc_dtype, out_dtype);
+    if (M == 0 || N == 0 || K == 0 || !tc_eligible(q))
+        return 0;
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess)
+        return -GEMM_ERR_CUDA;
+    if (auto_kernel(q, d.num_sms) < GEMM_KERNEL_TC_128x128)
+        return 0;
+    return few_tile_splits(M, N, K, d.num_sms);
 }
 
 extern "C" int gemm_ex_ws(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
@@ -360,6 +406,13 @@ extern "C" int gemm_ex_ws(const void* A, const void* B, void* C, int64_t M, int6
     if (device_info(&d) != cudaSuccess)
         return GEMM_ERR_CUDA;
     const int kernel = auto_kernel(q, d.num_sms);
+    if (workspace && kernel >= GEMM_KERNEL_TC_128x128) {
+        // Few output tiles and a long K: split K across the idle SMs.
+        const int splits = few_tile_splits(M, N, K, d.num_sms);
+        if (splits > 1 && workspace_bytes >= gemm_splitk_workspace_size(M, N, K, splits))
+            return gemm_splitk(A, B, C, M, N, K, splits, in_dtype, acc_dtype, out_dtype, workspace,
+                               workspace_bytes, stream);
+    }
     if (kernel != GEMM_KERNEL_TC_256x256 || !workspace)
         return run(q, kernel, s);
     TcLaunch l{};

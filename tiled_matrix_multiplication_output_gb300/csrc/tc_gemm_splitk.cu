@@ -104,20 +104,34 @@ __device__ __forceinline__ void add4(float4& a, const float4 b)
 }
 
 // C[i] = alpha * sum_s ws[s][i] + beta * C[i], four elements per step
-// (M * N is a multiple of 4 because N is).
+// (M * N is a multiple of 4 because N is).  The partials are added in split
+// order; the loads of eight splits are issued before they are added, so a
+// thread waits for memory once per eight splits rather than once per split.
 template <typename OutT>
 __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ ws, OutT* __restrict__ C, long long mn,
                          int splits, float alpha, float beta)
 {
+    constexpr int BATCH = 8;
     grid_dep_wait();
     const long long n4 = mn / 4;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += stride) {
-        float4 acc = load4(ws + 4 * i);
-        for (int s = 1; s < splits; ++s)
-            add4(acc, load4(ws + static_cast<long long>(s) * mn + 4 * i));
+        const float* src = ws + 4 * i;
+        float4 acc = load4(src);
+        int s = 1;
+        for (; s + BATCH <= splits; s += BATCH) {
+            float4 v[BATCH];
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j)
+                v[j] = load4(src + static_cast<long long>(s + j) * mn);
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j)
+                add4(acc, v[j]);
+        }
+        for (; s < splits; ++s)
+            add4(acc, load4(src + static_cast<long long>(s) * mn));
         finish4(C + 4 * i, acc, alpha, beta);
     }
 }
