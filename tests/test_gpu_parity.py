@@ -244,3 +244,31 @@ def test_automatic_choice_on_the_named_workloads():
     assert pick(96, 200, 1000, tg.BF16, tg.F32) == "tc_128x128"
     assert pick(4096, 4096, 4096, tg.F16, tg.F16, torch.float16) == "tc_256x256"
     assert pick(8192, 8192, 8192, tg.BF16, tg.BF16) == "tc_256x256"
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "f16"])
+def test_simt_large_tile_kernel_exact(in_dtype):
+    """Grids of at least one 128 x 128 tile per SM take the SIMT kernel's
+    large-tile form: ragged in every dimension (2051 x 1283 x 77: 17 x 11
+    tiles, 9 K tiles of 8 with a partial last one), integer inputs, every
+    output type; exact."""
+    A, B = inputs.draw(2051, 1283, 77, in_dtype, "int", seed=16)
+    assert 17 * 11 >= torch.cuda.get_device_properties(0).multi_processor_count
+    for out in OUT_TYPES:
+        expect_exact(run_gpu(A, B, out, "simt"), A, B)
+
+
+def test_simt_large_tile_kernel_transposed_and_addmm():
+    """The large-tile SIMT kernel with transposed operands and the
+    alpha/beta store, against the oracle's general form (integer inputs,
+    exact)."""
+    M, N, K = 2048, 1536, 40
+    A0, B0 = inputs.draw(M, N, K, "f32", "int", seed=17)
+    Cin = inputs.draw(M, 1, N, "f32", "int", seed=18)[0]          # an M x N integer matrix
+    for op_a, op_b in (("t", "n"), ("n", "t"), ("t", "t")):
+        A = A0.t().contiguous() if op_a == "t" else A0
+        B = B0.t().contiguous() if op_b == "t" else B0
+        C = tg.addmm(A.cuda(), B.cuda(), Cin.clone().cuda(), op_a=op_a, op_b=op_b, alpha=2.0,
+                     beta=-1.0, out_dtype=torch.float32, kernel="simt").cpu()
+        ref, _ = oracle.gemm_general(A, B, op_a, op_b, alpha=2.0, beta=-1.0, C_in=Cin)
+        np.testing.assert_array_equal(C.double().numpy(), ref)

@@ -178,10 +178,159 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
     }
 }
 
+// Large-tile variant for grids that fill the GPU: a 128 x 128 block tile,
+// K tiles of 8, and an 8 x 8 micro-tile per thread (256 threads).  A
+// thread's rows are {4 ty .. 4 ty + 3} and {64 + 4 ty .. 64 + 4 ty + 3} and
+// its columns likewise with tx, so each K step reads its 8 A and 8 B values
+// as four 16-byte shared-memory loads (64 FMAs per 4 loads, against 16 per 8
+// in the 4 x 4 kernel); a warp's B reads are 16 consecutive 16-byte words
+// and its A reads are broadcasts, so neither conflicts.  Staging, prefetch,
+// edge guards, transposed operands and the alpha/beta store are those of
+// simt_gemm_kernel.
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(256, 2)
+    simt_gemm_big_kernel(const InT* __restrict__ A, const InT* __restrict__ B, OutT* C, int M,
+                         int N, int K, int op_a, int op_b, float alpha, float beta)
+{
+    constexpr int BM = 128, BN = 128, BK = 8, NT = 256, PAD = 4;
+    constexpr int LA = BM * BK / NT, LB = BK * BN / NT;  // 4 and 4
+    __shared__ __align__(16) float As[BK][BM + PAD];
+    __shared__ __align__(16) float Bs[BK][BN + PAD];
+
+    const int tid = threadIdx.x;
+    const int tx = tid & 15;
+    const int ty = tid >> 4;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int tiles_m = (M + BM - 1) / BM;
+    const long long num_tiles = static_cast<long long>(tiles_m) * tiles_n;
+
+    // Per output tile, each thread's staged elements have fixed row (or
+    // column) offsets; a K tile only adds k0 times the K stride.
+    float ra[LA], rb[LB];
+    long long a_base[LA], b_base[LB];
+    int a_k[LA], b_k[LB];
+    bool a_in[LA], b_in[LB];
+    const long long a_kstride = op_a ? M : 1, b_kstride = op_b ? 1 : N;
+    auto set_tile = [&](int m0, int n0) {
+#pragma unroll
+        for (int r = 0; r < LA; ++r) {
+            const int e = tid + r * NT;
+            const int i = op_a ? e % BM : e / BK;
+            const int k = op_a ? e / BM : e % BK;
+            const int gm = m0 + i;
+            a_k[r] = k;
+            a_in[r] = gm < M;
+            a_base[r] = op_a ? static_cast<long long>(k) * M + gm : static_cast<long long>(gm) * K + k;
+        }
+#pragma unroll
+        for (int r = 0; r < LB; ++r) {
+            const int e = tid + r * NT;
+            const int k = op_b ? e % BK : e / BN;
+            const int j = op_b ? e / BK : e % BN;
+            const int gn = n0 + j;
+            b_k[r] = k;
+            b_in[r] = gn < N;
+            b_base[r] = op_b ? static_cast<long long>(gn) * K + k : static_cast<long long>(k) * N + gn;
+        }
+    };
+    auto load_tile = [&](int k0) {
+        const long long ka = static_cast<long long>(k0) * a_kstride;
+        const long long kb = static_cast<long long>(k0) * b_kstride;
+#pragma unroll
+        for (int r = 0; r < LA; ++r)
+            ra[r] = (a_in[r] && k0 + a_k[r] < K) ? to_f32(A[a_base[r] + ka]) : 0.0f;
+#pragma unroll
+        for (int r = 0; r < LB; ++r)
+            rb[r] = (b_in[r] && k0 + b_k[r] < K) ? to_f32(B[b_base[r] + kb]) : 0.0f;
+    };
+    auto store_tile = [&]() {
+#pragma unroll
+        for (int r = 0; r < LA; ++r) {
+            const int e = tid + r * NT;
+            As[op_a ? e / BM : e % BK][op_a ? e % BM : e / BK] = ra[r];
+        }
+#pragma unroll
+        for (int r = 0; r < LB; ++r) {
+            const int e = tid + r * NT;
+            Bs[op_b ? e % BK : e / BN][op_b ? e / BK : e % BN] = rb[r];
+        }
+    };
+
+    for (long long tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int m0 = static_cast<int>(tile / tiles_n) * BM;
+        const int n0 = static_cast<int>(tile % tiles_n) * BN;
+        float acc[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                acc[i][j] = 0.0f;
+
+        set_tile(m0, n0);
+        if (K > 0) {
+            load_tile(0);
+            store_tile();
+            __syncthreads();
+        }
+        for (int k0 = 0; k0 < K; k0 += BK) {
+            const bool more = k0 + BK < K;
+            if (more)
+                load_tile(k0 + BK);
+#pragma unroll
+            for (int k = 0; k < BK; ++k) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&As[k][4 * ty]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&As[k][64 + 4 * ty]);
+                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[k][4 * tx]);
+                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[k][64 + 4 * tx]);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            }
+            __syncthreads();
+            if (more) {
+                store_tile();
+                __syncthreads();
+            }
+        }
+
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int gm = m0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
+            if (gm >= M)
+                continue;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int gn = n0 + (j < 4 ? 4 * tx + j : 64 + 4 * tx + j - 4);
+                if (gn < N) {
+                    OutT* dst = C + static_cast<long long>(gm) * N + gn;
+                    const float v = (beta != 0.0f) ? fmaf(beta, load_out(dst), alpha * acc[i][j])
+                                                   : alpha * acc[i][j];
+                    store_out(dst, v);
+                }
+            }
+        }
+    }
+}
+
 template <int BM, int BN, int BK, int TM, int TN, typename InT, typename OutT>
 cudaError_t launch_simt(const SimtLaunch& l, cudaStream_t stream)
 {
     constexpr int NT = (BM / TM) * (BN / TN);
+    // Grids that fill every SM with 128 x 128 tiles take the large-tile kernel.
+    const long long big_tiles = static_cast<long long>((l.M + 127) / 128) * ((l.N + 127) / 128);
+    if (BM == 64 && big_tiles >= l.num_sms) {
+        const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 2;
+        const int grid = static_cast<int>(std::max<long long>(1, std::min(big_tiles, cap)));
+        note_launch();
+        simt_gemm_big_kernel<InT, OutT><<<grid, 256, 0, stream>>>(
+            static_cast<const InT*>(l.A), static_cast<const InT*>(l.B), static_cast<OutT*>(l.C),
+            l.M, l.N, l.K, l.op_a, l.op_b, l.alpha, l.beta);
+        return cudaGetLastError();
+    }
     const long long tiles = static_cast<long long>((l.M + BM - 1) / BM) * ((l.N + BN - 1) / BN);
     // Enough blocks for several resident per SM; each strides over tiles.
     const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 16;
