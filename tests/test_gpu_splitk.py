@@ -110,3 +110,34 @@ def test_gemm_ex_ws_splits_few_tile_products():
     assert rc == 0
     torch.cuda.synchronize()
     assert torch.equal(C, C2)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("shape", [(96, 200, 1000), (100, 136, 2056), (384, 256, 4096)])
+def test_gemm_ex_ws_few_tile_split_every_output_type(shape, out_dtype):
+    """The few-tile split path of gemm_ex_ws on ragged shapes and every output
+    type: exact on integer inputs, within the bound on random ones, and
+    identical run to run (the partials are added in a fixed order)."""
+    M, N, K = shape
+    code = {torch.float32: tg.F32, torch.float16: tg.F16, torch.bfloat16: tg.BF16}[out_dtype]
+    assert tg.gemm_ws_split_count(M, N, K, tg.F16, tg.F32, code) >= 2
+    s = torch.cuda.current_stream().cuda_stream
+    ws_bytes = tg.gemm_workspace_size(M, N, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    for dist in ("int", "normal"):
+        A, B = inputs.draw(M, N, K, "f16", dist, seed=33)
+        dA, dB = A.cuda(), B.cuda()
+        outs = []
+        for _ in range(2):
+            C = torch.empty((M, N), dtype=out_dtype, device="cuda")
+            assert tg.gemm_ex_ws(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, tg.F16, tg.F32,
+                                 code, ws.data_ptr(), ws_bytes, s) == 0
+            outs.append(C)
+        assert tg.gemm_device_status(s) == 0
+        assert torch.equal(outs[0].view(torch.uint8), outs[1].view(torch.uint8))
+        if dist == "int":
+            expect_exact(outs[0].cpu(), A, B)
+        else:
+            C_ref, Cabs = oracle.gemm(A, B)
+            tolerance_check(outs[0].cpu(), C_ref, Cabs,
+                            with_output_rounding=(out_dtype != torch.float32))
