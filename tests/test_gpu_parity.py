@@ -207,7 +207,7 @@ def test_host_buffer_entry_point_pipelined():
     own copy streams; the result is exact on integer inputs, and a second
     call right after the first (other inputs, same device buffers) sees its
     own inputs only."""
-    M, N, K = 4100, 520, 264            # 4 panels of 1280 rows, the last one ragged
+    M, N, K = 4100, 520, 264            # 5 panels of 1024 rows, the last one 4 rows
     s = torch.cuda.current_stream()
     dA = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
     dB = torch.empty(K, N, dtype=torch.bfloat16, device="cuda")

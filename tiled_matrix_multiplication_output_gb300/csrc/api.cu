@@ -506,8 +506,13 @@ extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host
     // Row panels of A and C: B is copied once, then the copy of A's panel
     // i + 1 and of C's panel i - 1 overlap the product of panel i.  Panels
     // are whole 256-row tile rows, at least 1024 rows; small products (or
-    // K == 0) run as one panel on the caller's stream.
-    int64_t panel = ((M + 3) / 4 + 255) / 256 * 256;
+    // K == 0) run as one panel on the caller's stream.  Eight panels rather
+    // than four shorten the last copy-compute-copy chain: 1.65 vs 1.74 ms for
+    // 8192^3 BF16 on GB300 (host links at about 210 GB/s each way).
+#ifndef TMMO_HOST_PANELS
+#define TMMO_HOST_PANELS 8
+#endif
+    int64_t panel = ((M + TMMO_HOST_PANELS - 1) / TMMO_HOST_PANELS + 255) / 256 * 256;
     if (panel < 1024)
         panel = 1024;
     const int64_t panels = (M + panel - 1) / panel;
