@@ -65,9 +65,12 @@ constexpr int TC_THREADS = 192;  // 6 warps
 constexpr int TC_EPI_WARP0 = 2;
 constexpr int TC_STAGING_BYTES = 4096;  // 32 rows x 128 bytes per warp buffer
 
-// KSUB 64-wide K steps share one shared-memory stage (one barrier wait and
-// one commit per KSUB * 4 MMAs); sub-step j of a stage sits at j * SUB_A /
-// j * SUB_B.
+// KSUB 64-wide K steps share one shared-memory stage, released by one commit
+// per KSUB * 4 MMAs; sub-step j of a stage sits at j * SUB_A / j * SUB_B.
+// Each sub-step has its own full barrier, so the MMAs of the first K step
+// start as soon as its copies land, while the stage's later copies are still
+// in flight (measured on GB300: 4.5 % less time at 8192^3 and 4096^3 than
+// one full barrier per stage).
 template <int CG, int BN, int STAGES, int KSUB = 1>
 struct TcLayout {
     static constexpr int SUB_A = TC_BM * TC_BK * 2;              // 16 KiB per K step
@@ -81,7 +84,7 @@ struct TcLayout {
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_STAGING = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_BAR = OFF_STAGING + 4 * 2 * TC_STAGING_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
+    static constexpr int NUM_BARS = 2 * STAGES + 5 + STAGES * (KSUB - 1);  // + full per later K step
     static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
@@ -328,6 +331,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    // Full barrier of K step j of a stage: step 0 uses full_bar, later steps
+    // their own, so the MMAs of a step can start before the stage's later
+    // steps have landed.
+    auto full_sub = [&](int s, int j) {
+        return j == 0 ? full_bar(s) : bar0 + 8u * (2 * STAGES + 5 + s * (KSUB - 1) + (j - 1));
+    };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
@@ -344,7 +353,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
+            for (int j = 0; j < KSUB; ++j)
+                mbar_init(full_sub(s, j), 1);
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -395,14 +405,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     // test hook (-1 in normal use): skip the stage holding that K step
                     if (p.fault_skip_kblock < kb0 || p.fault_skip_kblock >= kb0 + nsub) {
-                        const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
-                        if (leader)
-                            mbar_arrive_expect_tx(full_bar(stage), CG * nsub * L::SUB_BYTES);
+                        if (leader) {
+#pragma unroll
+                            for (int j = 0; j < KSUB; ++j) {
+                                if (j < nsub)
+                                    mbar_arrive_expect_tx(full_sub(stage, j), CG * L::SUB_BYTES);
+                                else
+                                    mbar_arrive(full_sub(stage, j));  // unused step: complete its phase
+                            }
+                        }
 #pragma unroll
                         for (int sub = 0; sub < KSUB; ++sub) {
                         if (sub >= nsub)
                             break;
                         const int kb = kb0 + sub;
+                        const uint32_t fb = (CG == 2) ? mapa_shared(full_sub(stage, sub), 0) : full_sub(stage, sub);
                         const uint32_t dA = sA + stage * L::A_STAGE + sub * L::SUB_A;
                         const uint32_t dB = sB + stage * L::B_STAGE + sub * L::SUB_B;
                         auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
@@ -444,8 +461,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (issued[s] == 0)
                         continue;
                     const uint32_t par = static_cast<uint32_t>(issued[s] - 1) & 1u;
-                    const long long t0 = clock64();
-                    while (!mbar_try_wait(full_bar(s), par) && clock64() - t0 < p.wait_budget) {
+                    for (int j = 0; j < KSUB; ++j) {
+                        const long long t0 = clock64();
+                        while (!mbar_try_wait(full_sub(s, j), par) && clock64() - t0 < p.wait_budget) {
+                        }
                     }
                 }
             }
@@ -472,15 +491,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb0 = w.kb_begin; kb0 < w.kb_end; kb0 += KSUB) {
                     const int nsub = min(KSUB, w.kb_end - kb0);
-                    if (!tc_wait(full_bar(stage), phase, watch)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
 #pragma unroll
                     for (int sub = 0; sub < KSUB; ++sub) {
                     if (sub >= nsub)
                         break;
+                    // this K step's operands have landed
+                    if (!tc_wait(full_sub(stage, sub), phase, watch)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     const uint32_t a0 = sA + stage * L::A_STAGE + sub * L::SUB_A;
                     const uint32_t b0 = sB + stage * L::B_STAGE + sub * L::SUB_B;
 #pragma unroll
@@ -498,6 +518,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                        (kb0 != w.kb_begin) || sub != 0 || k != 0);
                     }
                     }
+                    if (!ok)
+                        break;
                     if constexpr (CG == 2)
                         tc_commit_pair(empty_bar(stage), 0x3);
                     else
