@@ -64,6 +64,17 @@ constexpr int TC_UMMA_K = 16;    // K per tcgen05.mma for 16-bit inputs
 constexpr int TC_THREADS = 192;  // 6 warps
 constexpr int TC_EPI_WARP0 = 2;
 constexpr int TC_STAGING_BYTES = 4096;  // 32 rows x 128 bytes per warp buffer
+// Share of the next work item's main loop over which a finished tile's
+// stores are spread (percent).  Every CTA finishes its tile at about the
+// same time, and storing all of C's tiles at once delays the operand loads
+// of the next tiles; a gap after each strip's store spreads the writes out.
+// Measured on GB300 (BF16, the CTA-pair kernel, interleaved runs): 1-2 %
+// off 8192^3 and 4096^3, 5 % off 12288 x 12288 x 2048, 3 % off
+// 5120 x 5120 x 1024; spreading over 40 % or 60 % lost time at short K, and
+// staggering the four epilogue warps against each other did not help.
+#ifndef TMMO_STORE_SPREAD_PCT
+#define TMMO_STORE_SPREAD_PCT 25
+#endif
 
 // KSUB 64-wide K steps share one shared-memory stage, released by one commit
 // per KSUB * 4 MMAs; sub-step j of a stage sits at j * SUB_A / j * SUB_B.
@@ -591,6 +602,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     buf ^= 1;
                 }
             }
+            // Gap after each store, in clock cycles: the spread share of the
+            // next item's tensor time (2 * BN cycles per 64-wide K step: four
+            // MMAs of M = 128 rows per CTA and N = BN), per strip of this
+            // warp.  None after a CTA's last item.
+            long long gap = 0;
+            if (!SPLIT && !w.partial && t + num_units < p.num_work) {
+                const TcWork nx = tc_work(t + num_units, p);
+                gap = static_cast<long long>(nx.kb_end - nx.kb_begin) * 2 * BN *
+                      TMMO_STORE_SPREAD_PCT / 100 / (BN / STRIP);
+            }
 #pragma unroll 1
             for (int s = 0; s < BN / STRIP && (SPLIT || !w.partial); ++s) {
                 const int col0 = nb * BN + s * STRIP;
@@ -612,6 +633,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     else
                         tma_store_2d(&tmC, stg, col0, row0);
                     bulk_commit_group();
+                    const long long t0 = clock64();
+                    while (clock64() - t0 < gap) {
+                    }
                 }
                 buf ^= 1;
             }
