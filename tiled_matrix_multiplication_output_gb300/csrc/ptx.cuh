@@ -170,12 +170,6 @@ __device__ __forceinline__ void bulk_wait_group_read()
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-// Wait until every committed store group has completed.
-__device__ __forceinline__ void bulk_wait_group_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (TMA store, tcgen05).
 // Programmatic dependent launch.  launch_dependents lets a grid launched

@@ -649,8 +649,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     mbar_arrive(tb);
             }
         }
+        // Shared memory may be released once the stores have read it; the
+        // grid's completion covers their writes to global memory (a
+        // reduction launched as a programmatic dependent waits for it).
         if (lane == 0)
-            bulk_wait_group_all();
+            bulk_wait_group_read<0>();
         __syncwarp();
     }
 
