@@ -75,8 +75,11 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
 
     // The next K tile is read from global memory into registers (all of a
     // thread's loads in flight together) while the current one is used from
-    // shared memory; it is stored after the barrier that ends that use.
-    float ra[LA], rb[LB];
+    // shared memory; it is widened and stored after the barrier that ends
+    // that use (kept in the input type until then, so that no conversion
+    // waits for a load before the multiplies).
+    InT ra[LA], rb[LB];
+    const InT zero = static_cast<InT>(0.0f);
     auto load_tile = [&](int m0, int n0, int k0) {
         // A tile (BM x BK): consecutive threads walk the dimension that is
         // contiguous in memory (k for A as stored, m for A transposed).
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
             const int gm = m0 + i, gk = k0 + k;
             const long long off = op_a ? static_cast<long long>(gk) * M + gm
                                        : static_cast<long long>(gm) * K + gk;
-            ra[r] = (e < BM * BK && gm < M && gk < K) ? to_f32(A[off]) : 0.0f;
+            ra[r] = (e < BM * BK && gm < M && gk < K) ? A[off] : zero;
         }
         // B tile (BK x BN): n contiguous for B as stored, k for B transposed.
 #pragma unroll
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
             const int gk = k0 + k, gn = n0 + j;
             const long long off = op_b ? static_cast<long long>(gn) * K + gk
                                        : static_cast<long long>(gk) * N + gn;
-            rb[r] = (e < BK * BN && gk < K && gn < N) ? to_f32(B[off]) : 0.0f;
+            rb[r] = (e < BK * BN && gk < K && gn < N) ? B[off] : zero;
         }
     };
     auto store_tile = [&]() {
@@ -107,13 +110,13 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
         for (int r = 0; r < LA; ++r) {
             const int e = tid + r * NT;
             if (e < BM * BK)
-                As[op_a ? e / BM : e % BK][op_a ? e % BM : e / BK] = ra[r];
+                As[op_a ? e / BM : e % BK][op_a ? e % BM : e / BK] = to_f32(ra[r]);
         }
 #pragma unroll
         for (int r = 0; r < LB; ++r) {
             const int e = tid + r * NT;
             if (e < BK * BN)
-                Bs[op_b ? e % BK : e / BN][op_b ? e / BK : e % BN] = rb[r];
+                Bs[op_b ? e % BK : e / BN][op_b ? e / BK : e % BN] = to_f32(rb[r]);
         }
     };
 
@@ -206,7 +209,8 @@ __global__ void __launch_bounds__(256, 2)
 
     // Per output tile, each thread's staged elements have fixed row (or
     // column) offsets; a K tile only adds k0 times the K stride.
-    float ra[LA], rb[LB];
+    InT ra[LA], rb[LB];  // raw until stored, as in simt_gemm_kernel
+    const InT zero = static_cast<InT>(0.0f);
     long long a_base[LA], b_base[LB];
     int a_k[LA], b_k[LB];
     bool a_in[LA], b_in[LB];
@@ -238,21 +242,21 @@ __global__ void __launch_bounds__(256, 2)
         const long long kb = static_cast<long long>(k0) * b_kstride;
 #pragma unroll
         for (int r = 0; r < LA; ++r)
-            ra[r] = (a_in[r] && k0 + a_k[r] < K) ? to_f32(A[a_base[r] + ka]) : 0.0f;
+            ra[r] = (a_in[r] && k0 + a_k[r] < K) ? A[a_base[r] + ka] : zero;
 #pragma unroll
         for (int r = 0; r < LB; ++r)
-            rb[r] = (b_in[r] && k0 + b_k[r] < K) ? to_f32(B[b_base[r] + kb]) : 0.0f;
+            rb[r] = (b_in[r] && k0 + b_k[r] < K) ? B[b_base[r] + kb] : zero;
     };
     auto store_tile = [&]() {
 #pragma unroll
         for (int r = 0; r < LA; ++r) {
             const int e = tid + r * NT;
-            As[op_a ? e / BM : e % BK][op_a ? e % BM : e / BK] = ra[r];
+            As[op_a ? e / BM : e % BK][op_a ? e % BM : e / BK] = to_f32(ra[r]);
         }
 #pragma unroll
         for (int r = 0; r < LB; ++r) {
             const int e = tid + r * NT;
-            Bs[op_b ? e % BK : e / BN][op_b ? e / BK : e % BN] = rb[r];
+            Bs[op_b ? e % BK : e / BN][op_b ? e / BK : e % BN] = to_f32(rb[r]);
         }
     };
 
