@@ -54,16 +54,24 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
                  : "memory");
 }
 
+// A thread in try_wait may be suspended until the phase completes, or until
+// this many nanoseconds pass (the instruction's suspend-time hint).  A long
+// limit keeps waiting threads off the issue slots: measured on GB300 it cut
+// this kernel's executed instructions and raised the power-capped 8192^3
+// rate by 0.6 %; the thread still resumes as soon as the phase completes.
+// Callers bound their waits by a clock budget checked between attempts.
+constexpr uint32_t MBAR_SUSPEND_HINT_NS = 1000000;
+
 // True once the phase with parity `parity` has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(MBAR_SUSPEND_HINT_NS)
         : "memory");
     return ok != 0;
 }
@@ -74,10 +82,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(MBAR_SUSPEND_HINT_NS)
         : "memory");
     return ok != 0;
 }
