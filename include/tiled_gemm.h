@@ -184,7 +184,7 @@ int gemm_ex_ws(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
  * splits), or 0 when it does not.  The rule: a tensor-core product whose
  * 128 x 128 output tiles occupy at most a quarter of the SMs, with K of at
  * least 512, is split so that up to one unit of work runs per SM, into at
- * most 16 ranges.  gemm_ex_ws does so only when its workspace holds
+ * most 8 ranges.  gemm_ex_ws does so only when its workspace holds
  * gemm_splitk_workspace_size(M, N, K, count) bytes, which
  * gemm_workspace_size always covers.  There is no counterpart in the pages:
  * they accumulate each tile over all of K in one place.  Returns the count,
