@@ -1,0 +1,88 @@
+"""Host logic of bench.py, without a GPU: which workloads flush L2 between
+steps, the tie between committed ncu counters and the kernel sources, the
+clock-sample parsing behind the "clocks" key, and the whole-job rate."""
+import os
+import tempfile
+
+import pytest
+
+import bench
+from tiled_matrix_multiplication_output_gb300 import inputs
+
+
+def test_l2_flush_rule_on_the_named_workloads():
+    # A + B + C of the four smaller workloads fit in the 129 MB L2 (4096^3 FP16:
+    # 96 MiB), so their steps run with L2 overwritten in between; 8192^3 BF16
+    # (384 MiB) streams from HBM on its own.
+    for name in ("worked_9x9", "square_128_f16", "edge_96x200x1000_bf16", "square_4096_f16"):
+        assert bench.needs_flush(inputs.WORKLOADS[name]), name
+    w = inputs.WORKLOADS["square_8192_bf16"]
+    assert bench.footprint_bytes(w) == 3 * 8192 * 8192 * 2
+    assert not bench.needs_flush(w)
+    assert "flushed" in bench.config_of(inputs.WORKLOADS["square_128_f16"], "k")["l2"]
+    assert bench.config_of(w, "k")["l2"] == "A+B+C larger than L2"
+
+
+def test_committed_traffic_is_tied_to_the_kernel_sources(tmp_path, monkeypatch):
+    # the committed summary of the benchmarked kernel matches today's sources
+    got = bench.committed_traffic("tc_gemm_256x256", "square_8192_bf16")
+    assert isinstance(got, int) and got > 3 * 8192 * 8192 * 2 // 2
+    # a summary taken from other sources is ignored
+    (tmp_path / "k_w.md").write_text("- dram_bytes_per_launch: 123\n- source_sha256: `00`\n")
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    assert bench.committed_traffic("k", "w") is None
+    (tmp_path / "k_w.md").write_text(
+        f"- dram_bytes_per_launch: 123\n- source_sha256: `{bench.source_digest()}`\n")
+    assert bench.committed_traffic("k", "w") == 123
+    assert bench.committed_traffic("k", "missing") is None
+
+
+class _DoneProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sampler_with(rows):
+    s = bench.ClockSampler(0)
+    s.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+    s.tmp.write("\n".join(rows) + "\n")
+    s.tmp.flush()
+    s.proc = _DoneProc()
+    return s
+
+
+def test_clock_sampler_parsing():
+    not_active = "Not Active"
+    rows = [
+        # idx, sm, max, power, active mask, hw_slow, hw_thermal, sw_thermal, sw_power_cap
+        f"0, 345, 2070, 150.0, 0x0, {not_active}, {not_active}, {not_active}, {not_active}",
+        f"0, 1470, 2070, 1370.0, 0x4, {not_active}, {not_active}, {not_active}, Active",
+        f"0, 1455, 2070, 1371.0, 0x4, {not_active}, {not_active}, {not_active}, Active",
+        f"0, 1481, 2070, 1369.0, 0x4, {not_active}, {not_active}, {not_active}, Active",
+        "garbage line",
+    ]
+    got = _sampler_with(rows).stop()
+    # the idle sample (below half the highest clock) is left out of the median
+    assert got == {"sm_mhz": 1470.0, "sm_max_mhz": 2070.0, "samples": 4,
+                   "reasons": ["sw_power_cap"]}
+    hot = _sampler_with([f"0, 900, 2070, 500.0, 0x40, Active, {not_active}, Active, {not_active}"])
+    assert hot.stop()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    assert _sampler_with(["nothing useful"]).stop() is None
+    assert bench.ClockSampler(0).stop() is None   # never started (no nvidia-smi)
+
+
+def test_job_rate_counts_every_rank():
+    flops = 2.0 * 8192 ** 3
+    one = bench.job_rate(flops, 10, 1, 6.5)
+    assert one == pytest.approx(flops * 10 / 6.5e-3 / 1e12)
+    # two replicas in the same (slowest-rank) time: twice the job's rate
+    assert bench.job_rate(flops, 10, 2, 6.5) == pytest.approx(2 * one)
+
+
+def test_source_digest_covers_the_kernel_files():
+    for name in bench.KERNEL_SOURCES:
+        assert os.path.exists(os.path.join(bench.CSRC, name)), name
+    assert len(bench.source_digest()) == 64
