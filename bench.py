@@ -7,7 +7,8 @@ L2, so consecutive steps cannot reuse inputs from L2.  Smaller workloads
 (--workload) overwrite L2 between steps, outside each step's own events.
 
 Prints ONE JSON line (rank 0).  Keys beyond the common ones:
-  roofline      dominant kernel vs the measured dense BF16 tensor peak
+  roofline      dominant kernel vs the measured dense BF16 tensor peak, or vs the
+                measured HBM copy bandwidth for workloads below the ridge point
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
   e2e           the same metric through gemm_ex_host with pinned host
                 buffers (host-to-device copies of A, B and the device-to-host
@@ -270,6 +271,7 @@ def run_reference(args, rank, world):
 
 
 L2_BYTES = 129e6   # GB300 L2 capacity
+ALU_SMS = 152      # GB300 SMs, for the FP32 FMA peak
 
 
 def footprint_bytes(w):
@@ -282,6 +284,40 @@ def needs_flush(w) -> bool:
     """Whether A, B and C together fit in L2, so that consecutive steps would
     find their inputs there: such workloads flush L2 between steps."""
     return footprint_bytes(w) <= L2_BYTES
+
+
+def roofline_of(w, flops, avg_launch_ms, peaks, peak_kind, traffic):
+    """The roofline object for one workload.  The bound follows from the
+    arithmetic intensity (FLOPs per compulsory byte of A, B and C) against
+    the ridge point of the compute peak over the HBM peak: below it the
+    workload is HBM-bound (achieved = compulsory bytes / time, against the
+    measured copy bandwidth), above it compute-bound -- the tensor cores for
+    16-bit inputs (measured cuBLAS BF16 peak), the FP32 FMA pipes for FP32
+    inputs (peak derived: SMs x 128 lanes x 2 FLOP x the maximum SM clock)."""
+    seconds = avg_launch_ms * 1e-3
+    nbytes = footprint_bytes(w)
+    hbm = float(peaks["hbm_gbs"])
+    if w.in_dtype == "f32":
+        compute, kind = ALU_SMS * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12, "alu"
+        source = f"derived: {ALU_SMS} SMs x 128 FP32 lanes x 2 FLOP x the maximum SM clock"
+    else:
+        compute, kind = float(peaks["bf16_tflops"]), "tensor"
+        source = f"{peak_kind} bf16_tflops (burst)"
+    timing = ("CUDA events around every step on the launching stream; a step is the main "
+              "kernel plus, when tiles are split, the small reduction, so the main kernel's "
+              "share is slightly understated")
+    if flops / nbytes < compute * 1e12 / (hbm * 1e9):
+        achieved = nbytes / seconds / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic, "timing": timing,
+                "algorithmic_bytes": nbytes, "peak_source": f"{peak_kind} hbm_gbs"}
+    achieved = flops / seconds / 1e12
+    line = {"bound": kind, "achieved": achieved, "peak": compute, "unit": UNIT,
+            "frac": achieved / compute, "traffic": traffic, "timing": timing,
+            "peak_source": source}
+    if kind == "tensor":
+        line["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+    return line
 
 
 def config_of(w, kernel):
@@ -441,8 +477,6 @@ def run_ours(args, rank, world, local):
         return
     peaks, peak_kind = load_peaks()
     avg_launch_ms = statistics.mean(per_launch)
-    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops"])
     base_kernel = kname.split("+")[0]
     traffic = committed_traffic(
         f"tc_gemm_{base_kernel[3:]}" if base_kernel.startswith("tc_") else base_kernel, w.name)
@@ -451,13 +485,7 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.in_dtype, "data": "synthetic",
         "config": config_of(w, kname),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "timing": "CUDA events around every step on the launching stream; a step "
-                               "is the main kernel plus, when tiles are split, the small tail "
-                               "reduction, so the main kernel's share is slightly understated",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_kind} bf16_tflops (burst)",
-                     "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"])},
+        "roofline": roofline_of(w, flops, avg_launch_ms, peaks, peak_kind, traffic),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": (w.M * w.K + w.K * w.N) * in_b,
                 "d2h_bytes_per_step": w.M * w.N * out_b, "steps": e2e_steps,
                 "entry_point": "gemm_ex_host (pinned host buffers)"},

@@ -86,3 +86,39 @@ def test_source_digest_covers_the_kernel_files():
     for name in bench.KERNEL_SOURCES:
         assert os.path.exists(os.path.join(bench.CSRC, name)), name
     assert len(bench.source_digest()) == 64
+
+
+PEAKS = {"hbm_gbs": 6754.8, "bf16_tflops": 1957.5, "bf16_tflops_sustained": 1745.9,
+         "sm_max_mhz": 2070.0}
+
+
+def _flops(w):
+    return 2.0 * w.M * w.N * w.K
+
+
+@pytest.mark.parametrize("name, bound", [
+    ("worked_9x9", "hbm"),               # 1.5 FLOP/B
+    ("square_128_f16", "hbm"),           # 32 FLOP/B
+    ("edge_96x200x1000_bf16", "hbm"),    # 57 FLOP/B
+    ("square_4096_f16", "tensor"),       # 1365 FLOP/B, ridge about 290
+    ("square_8192_bf16", "tensor"),      # 2731 FLOP/B
+])
+def test_roofline_bound_follows_arithmetic_intensity(name, bound):
+    w = inputs.WORKLOADS[name]
+    r = bench.roofline_of(w, _flops(w), 0.01, PEAKS, "measured", None)
+    assert r["bound"] == bound
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    if bound == "hbm":
+        assert r["unit"] == "GB/s" and r["peak"] == 6754.8
+        assert r["achieved"] == pytest.approx(bench.footprint_bytes(w) / 1e-5 / 1e9)
+    else:
+        assert r["unit"] == "TFLOP/s" and r["peak"] == 1957.5
+        assert r["achieved"] == pytest.approx(_flops(w) / 1e-5 / 1e12)
+        assert r["frac_of_sustained"] == pytest.approx(r["achieved"] / 1745.9)
+
+
+def test_roofline_fp32_compute_bound_is_the_fma_pipes():
+    w = inputs.Workload("f32_4096", 4096, 4096, 4096, "f32", "f32", "normal", 0)
+    r = bench.roofline_of(w, _flops(w), 3.0, PEAKS, "measured", None)
+    assert r["bound"] == "alu"
+    assert r["peak"] == pytest.approx(152 * 128 * 2 * 2070e6 / 1e12)
