@@ -82,3 +82,18 @@ def test_workspace_size_bound():
     props = torch.cuda.get_device_properties(0)
     assert n == (props.multi_processor_count // 2) * 256 * 256 * 4
     assert tg.gemm_workspace_size(0, 8, 8) == 0
+
+
+def test_workspace_path_shape_fuzz_exact():
+    """gemm_ex_ws on 12 seeded random shapes (M, N up to 2600, K up to 1200,
+    every output type): whatever it picks -- whole waves, a split last wave,
+    few-tile split-K or another tile shape -- the result is exact on integer
+    inputs."""
+    rng = np.random.default_rng(2026)
+    odts = [torch.float32, torch.float16, torch.bfloat16]
+    for i in range(12):
+        M = int(rng.integers(25, 326)) * 8
+        N = int(rng.integers(25, 326)) * 8
+        K = int(rng.integers(8, 151)) * 8
+        A, B = inputs.draw(M, N, K, "bf16" if i % 2 else "f16", "int", seed=200 + i)
+        expect_exact(_ws(A, B, odts[i % 3]), A, B)
