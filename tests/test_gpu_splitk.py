@@ -78,9 +78,9 @@ def test_splitk_unaligned_falls_back_exactly():
 
 def test_gemm_ex_ws_splits_few_tile_products():
     """gemm_ex_ws takes split-K for few output tiles and a long K (the
-    96 x 200 x 1000 workload's shape): same partial order as gemm_splitk
-    with the reported count, exact on integer inputs, two launches; large
-    products and short K are not split."""
+    96 x 200 x 1000 workload's shape): two launches, bit for bit the result
+    of gemm_splitk with the reported count, on integer and on random inputs;
+    large products and short K are not split."""
     M, N, K = 96, 200, 1000
     count = tg.gemm_ws_split_count(M, N, K, tg.BF16, tg.F32, tg.F32)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -104,12 +104,18 @@ def test_gemm_ex_ws_splits_few_tile_products():
     assert tg.gemm_device_status(s) == 0
     expect_exact(C.cpu(), A, B)
     ws2 = torch.empty(tg.gemm_splitk_workspace_size(M, N, K, count), dtype=torch.uint8, device="cuda")
-    C2 = torch.empty((M, N), device="cuda")
-    rc = tg.gemm_splitk(dA.data_ptr(), dB.data_ptr(), C2.data_ptr(), M, N, K, count, tg.BF16,
-                        tg.F32, tg.F32, ws2.data_ptr(), ws2.numel(), s)
-    assert rc == 0
-    torch.cuda.synchronize()
-    assert torch.equal(C, C2)
+    for dist in ("int", "normal"):
+        A, B = inputs.draw(M, N, K, "bf16", dist, seed=32)
+        dA, dB = A.cuda(), B.cuda()
+        C = torch.empty((M, N), device="cuda")
+        C2 = torch.empty((M, N), device="cuda")
+        assert tg.gemm_ex_ws(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, tg.BF16, tg.F32,
+                             tg.F32, ws.data_ptr(), ws_bytes, s) == 0
+        rc = tg.gemm_splitk(dA.data_ptr(), dB.data_ptr(), C2.data_ptr(), M, N, K, count, tg.BF16,
+                            tg.F32, tg.F32, ws2.data_ptr(), ws2.numel(), s)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(torch.int32), C2.view(torch.int32)), dist
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
