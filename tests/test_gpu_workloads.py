@@ -109,3 +109,24 @@ def test_tall_product_many_tiles():
         half_ulp = HALF_ULP[torch.bfloat16] * np.abs(ref)
         assert np.all(np.abs(got - ref) <= oracle.tolerance(ref_abs) + half_ulp)
         _sums_check(C, A, B)
+
+
+@pytest.mark.parametrize("M, N, K, out_dtype", [
+    (2097152, 64, 64, torch.float32),      # 2^21 rows: 16384 tile rows, TMA row coordinates to 2^21
+    (64, 2097152, 64, torch.bfloat16),     # 2^21 columns
+    (128, 128, 1048576, torch.float32),    # 2^20 K steps of one element: one tile, 16384 K steps
+])
+def test_extreme_dimensions_sampled_exact(M, N, K, out_dtype):
+    """Dimensions far beyond the named workloads, on the automatic choice and
+    on gemm_ex_ws (split-K for the long-K case): integer inputs in [-1, 1]
+    keep every sum exact in FP32 (|C| <= K <= 2^20), so sampled entries --
+    every tile edge included -- must equal the oracle's, rounded to the
+    output type."""
+    A, B = inputs.draw(M, N, K, "bf16", "int", seed=40, lo=-1, hi=1)
+    rows, cols = sample_indices(M, N, 3000, seed=41)
+    ref, _ = oracle.gemm_entries(A, B, rows, cols)
+    want = oracle.round_to(ref, out_dtype).double().numpy()
+    for C in (run_gpu(A, B, out_dtype, "auto"),
+              tg.matmul_ws(A.cuda(), B.cuda(), out_dtype=out_dtype).cpu()):
+        got = C[torch.from_numpy(rows), torch.from_numpy(cols)].double().numpy()
+        np.testing.assert_array_equal(got, want)
