@@ -88,6 +88,19 @@ def test_job_rate_counts_every_rank():
     assert bench.job_rate(flops, 10, 2, 6.5) == pytest.approx(2 * one)
 
 
+def test_reference_block_keeps_every_core_busy_within_the_step_budget():
+    # 8192^3 at 2000 + 20 steps on 16 cores: 0.06 s per step, 27 us per entry
+    rows, cols = bench.reference_block(8192, 8192, 16, 27e-6, 120.0 / 2020)
+    assert rows == 16 and 1 <= cols < 8192
+    assert cols * 27e-6 <= 120.0 / 2020
+    # a generous budget widens to full rows, then adds rows by the thread count
+    rows, cols = bench.reference_block(8192, 8192, 16, 27e-6, 2.0)
+    assert cols == 8192 and rows % 16 == 0 and rows * 8192 * 27e-6 / 16 <= 2.0
+    # never beyond C, never empty
+    assert bench.reference_block(9, 9, 16, 1e-9, 100.0) == (9, 9)
+    assert bench.reference_block(4, 3, 16, 10.0, 1e-3) == (4, 1)
+
+
 def test_source_digest_covers_the_kernel_files():
     for name in bench.KERNEL_SOURCES:
         assert os.path.exists(os.path.join(bench.CSRC, name)), name
