@@ -16,8 +16,10 @@
  *
  * Memory and ownership.  A, B and C are device pointers owned by the caller
  * (except where an entry point says "host").  The library allocates no
- * device memory per call; its only state is one device status word per GPU
- * and a cached driver entry point.
+ * device memory per call.  Its state: one device status word per GPU, a
+ * cached driver entry point, the fixed scratch array of gemm_splitk_noalloc
+ * (on every GPU that loads the library) and the two copy streams that
+ * gemm_ex_host creates once per device.
  *
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  * default stream).  Calls are stream-ordered and asynchronous: they return
@@ -231,9 +233,9 @@ int gemm_splitk(const void* A, const void* B, void* C, int64_t M, int64_t N, int
  * device memory; it allocates nothing.  The pages have no counterpart: this
  * entry point exists for deployment, not for the method.
  *
- * Who needs it: code whose product is recorded into a CUDA graph or runs
- * inside a framework that owns every allocation, real-time paths where a
- * cudaMalloc (which may synchronize the device) is not allowed, and
+ * Who needs it: code that runs inside a framework owning every device
+ * allocation (its pool may already hold all free memory), real-time paths
+ * where a cudaMalloc (which may synchronize the device) is not allowed, and
  * services that reserve all device memory up front.  Instead of a caller
  * workspace, the FP32 partials live in one fixed array inside the library,
  * GEMM_SPLITK_NOALLOC_MAX_BYTES on every GPU that loads the library, kept

@@ -1,6 +1,7 @@
 """gemm_splitk_noalloc: split-K for callers that cannot allocate device
-memory (graph-captured or framework-owned code, real-time paths, services
-that reserve all memory up front).  Its partials live in the library's fixed
+memory (code under a framework that owns every allocation, real-time paths
+where cudaMalloc may synchronize the device, services that reserve all
+memory up front).  Its partials live in the library's fixed
 scratch array instead of a caller workspace.
 
 Checked through the C ABI against the existing entry point, gemm_splitk with

@@ -636,10 +636,10 @@ extern "C" const char* gemm_error_string(int status)
 // Split-K without any allocation.
 //
 // Some callers cannot allocate device memory at the point where they need a
-// product: code recorded into a CUDA graph or running under a framework that
-// owns every allocation, real-time paths that must not call cudaMalloc (it
-// can synchronize the device and take milliseconds), and memory-budgeted
-// services that reserve all device memory up front.  For them,
+// product: code running under a framework that owns every allocation (its
+// pool may already hold all free memory), real-time paths that must not
+// call cudaMalloc (it can synchronize the device and take milliseconds),
+// and memory-budgeted services that reserve all device memory up front.  For them,
 // gemm_splitk_noalloc keeps its FP32 partials in the library's own
 // fixed-size device array below instead of a caller workspace.
 namespace tmmo {
