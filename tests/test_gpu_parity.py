@@ -272,3 +272,22 @@ def test_simt_large_tile_kernel_transposed_and_addmm():
                      beta=-1.0, out_dtype=torch.float32, kernel="simt").cpu()
         ref, _ = oracle.gemm_general(A, B, op_a, op_b, alpha=2.0, beta=-1.0, C_in=Cin)
         np.testing.assert_array_equal(C.double().numpy(), ref)
+
+
+@pytest.mark.parametrize("op_a,op_b", [("n", "n"), ("t", "n"), ("n", "t"), ("t", "t")])
+def test_simt_large_tile_kernel_layouts_ragged_k_tiles(op_a, op_b):
+    """The large-tile SIMT kernel in every operand layout, ragged in M, N
+    and K, with 1, 2, 3 and 10 K tiles of 8: the counts at which its
+    register prefetch (one K tile ahead, or two ahead for A transposed with
+    B as stored) starts, runs and drains differently.  Integer inputs,
+    exact against the oracle's general form; FP16 inputs on one case."""
+    M, N = 2051, 1283
+    for K, in_dtype, seed in ((5, "f32", 40), (13, "f32", 41), (21, "f32", 42),
+                              (77, "f32", 43), (21, "f16", 44)):
+        A0, B0 = inputs.draw(M, N, K, in_dtype, "int", seed=seed)
+        A = A0.t().contiguous() if op_a == "t" else A0
+        B = B0.t().contiguous() if op_b == "t" else B0
+        C = tg.addmm(A.cuda(), B.cuda(), op_a=op_a, op_b=op_b, out_dtype=torch.float32,
+                     kernel="simt").cpu()
+        ref, _ = oracle.gemm_general(A, B, op_a, op_b)
+        np.testing.assert_array_equal(C.double().numpy(), ref, err_msg=f"K={K} {in_dtype}")

@@ -190,15 +190,18 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
 // and its A reads are broadcasts, so neither conflicts.  Staging, prefetch,
 // edge guards, transposed operands and the alpha/beta store are those of
 // simt_gemm_kernel.
-template <typename InT, typename OutT>
+template <typename InT, typename OutT, bool OP_A, bool OP_B>
 __global__ void __launch_bounds__(256, 2)
     simt_gemm_big_kernel(const InT* __restrict__ A, const InT* __restrict__ B, OutT* C, int M,
-                         int N, int K, int op_a, int op_b, float alpha, float beta)
+                         int N, int K, float alpha, float beta)
 {
+    constexpr bool op_a = OP_A, op_b = OP_B;  // operand layouts fixed at compile time
     constexpr int BM = 128, BN = 128, BK = 8, NT = 256, PAD = 4;
     constexpr int LA = BM * BK / NT, LB = BK * BN / NT;  // 4 and 4
-    __shared__ __align__(16) float As[BK][BM + PAD];
-    __shared__ __align__(16) float Bs[BK][BN + PAD];
+    // Two shared tiles: the K tile being multiplied and the next one, so a
+    // single barrier per K tile separates a tile's stores from its reads.
+    __shared__ __align__(16) float As[2][BK][BM + PAD];
+    __shared__ __align__(16) float Bs[2][BK][BN + PAD];
 
     const int tid = threadIdx.x;
     const int tx = tid & 15;
@@ -207,57 +210,63 @@ __global__ void __launch_bounds__(256, 2)
     const int tiles_m = (M + BM - 1) / BM;
     const long long num_tiles = static_cast<long long>(tiles_m) * tiles_n;
 
-    // Per output tile, each thread's staged elements have fixed row (or
-    // column) offsets; a K tile only adds k0 times the K stride.
+    // A thread stages elements tid + 256 r (r < 4) of each tile, counted
+    // along the dimension that is contiguous in memory.  For A as stored
+    // (M x K) element r is at row tid / 8 + 32 r, k = tid % 8; for A stored
+    // transposed (K x M) at row tid % 128, k = tid / 128 + 2 r; B likewise,
+    // with columns for rows.  So element r lies a fixed distance from
+    // element 0 (32 rows or 2 k), and one offset plus one stride per operand
+    // address all four.
+    const int a_i = op_a ? tid % BM : tid / BK;  // tile row of element 0
+    const int a_k = op_a ? tid / BM : tid % BK;  // tile k of element 0
+    const int a_di = op_a ? 0 : NT / BK;         // rows from one element to the next
+    const int a_dk = op_a ? NT / BM : 0;         // k from one element to the next
+    const long long a_rs = op_a ? static_cast<long long>(a_dk) * M
+                                : static_cast<long long>(a_di) * K;
+    const long long a_ks = op_a ? M : 1;         // global distance of one k
+    const int b_j = op_b ? tid / BK : tid % BN;
+    const int b_k = op_b ? tid % BK : tid / BN;
+    const int b_dj = op_b ? NT / BK : 0;
+    const int b_dk = op_b ? 0 : NT / BN;
+    const long long b_rs = op_b ? static_cast<long long>(b_dj) * K
+                                : static_cast<long long>(b_dk) * N;
+    const long long b_ks = op_b ? 1 : N;
+
     InT ra[LA], rb[LB];  // raw until stored, as in simt_gemm_kernel
     const InT zero = static_cast<InT>(0.0f);
-    long long a_base[LA], b_base[LB];
-    int a_k[LA], b_k[LB];
-    bool a_in[LA], b_in[LB];
-    const long long a_kstride = op_a ? M : 1, b_kstride = op_b ? 1 : N;
+    long long a_off = 0, b_off = 0;  // global offset of element 0 at k = 0
+    unsigned a_rows = 0, b_cols = 0; // bit r: element r's row (column) is inside C
     auto set_tile = [&](int m0, int n0) {
-#pragma unroll
-        for (int r = 0; r < LA; ++r) {
-            const int e = tid + r * NT;
-            const int i = op_a ? e % BM : e / BK;
-            const int k = op_a ? e / BM : e % BK;
-            const int gm = m0 + i;
-            a_k[r] = k;
-            a_in[r] = gm < M;
-            a_base[r] = op_a ? static_cast<long long>(k) * M + gm : static_cast<long long>(gm) * K + k;
-        }
-#pragma unroll
-        for (int r = 0; r < LB; ++r) {
-            const int e = tid + r * NT;
-            const int k = op_b ? e % BK : e / BN;
-            const int j = op_b ? e / BK : e % BN;
-            const int gn = n0 + j;
-            b_k[r] = k;
-            b_in[r] = gn < N;
-            b_base[r] = op_b ? static_cast<long long>(gn) * K + k : static_cast<long long>(k) * N + gn;
-        }
-    };
-    auto load_tile = [&](int k0) {
-        const long long ka = static_cast<long long>(k0) * a_kstride;
-        const long long kb = static_cast<long long>(k0) * b_kstride;
+        const int gm = m0 + a_i;
+        a_off = op_a ? static_cast<long long>(a_k) * M + gm : static_cast<long long>(gm) * K + a_k;
+        a_rows = 0;
 #pragma unroll
         for (int r = 0; r < LA; ++r)
-            ra[r] = (a_in[r] && k0 + a_k[r] < K) ? A[a_base[r] + ka] : zero;
+            a_rows |= (gm + r * a_di < M ? 1u : 0u) << r;
+        const int gn = n0 + b_j;
+        b_off = op_b ? static_cast<long long>(gn) * K + b_k : static_cast<long long>(b_k) * N + gn;
+        b_cols = 0;
 #pragma unroll
         for (int r = 0; r < LB; ++r)
-            rb[r] = (b_in[r] && k0 + b_k[r] < K) ? B[b_base[r] + kb] : zero;
+            b_cols |= (gn + r * b_dj < N ? 1u : 0u) << r;
     };
-    auto store_tile = [&]() {
+    auto load_tile = [&](int k0) {
+        const long long ka = a_off + static_cast<long long>(k0) * a_ks;
+        const long long kb = b_off + static_cast<long long>(k0) * b_ks;
 #pragma unroll
-        for (int r = 0; r < LA; ++r) {
-            const int e = tid + r * NT;
-            As[op_a ? e / BM : e % BK][op_a ? e % BM : e / BK] = to_f32(ra[r]);
-        }
+        for (int r = 0; r < LA; ++r)
+            ra[r] = ((a_rows >> r) & 1u) && k0 + a_k + r * a_dk < K ? A[ka + r * a_rs] : zero;
 #pragma unroll
-        for (int r = 0; r < LB; ++r) {
-            const int e = tid + r * NT;
-            Bs[op_b ? e % BK : e / BN][op_b ? e / BK : e % BN] = to_f32(rb[r]);
-        }
+        for (int r = 0; r < LB; ++r)
+            rb[r] = ((b_cols >> r) & 1u) && k0 + b_k + r * b_dk < K ? B[kb + r * b_rs] : zero;
+    };
+    auto store_tile = [&](int buf) {
+#pragma unroll
+        for (int r = 0; r < LA; ++r)
+            As[buf][a_k + r * a_dk][a_i + r * a_di] = to_f32(ra[r]);
+#pragma unroll
+        for (int r = 0; r < LB; ++r)
+            Bs[buf][b_k + r * b_dk][b_j + r * b_dj] = to_f32(rb[r]);
     };
 
     for (long long tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -270,22 +279,14 @@ __global__ void __launch_bounds__(256, 2)
             for (int j = 0; j < 8; ++j)
                 acc[i][j] = 0.0f;
 
-        set_tile(m0, n0);
-        if (K > 0) {
-            load_tile(0);
-            store_tile();
-            __syncthreads();
-        }
-        for (int k0 = 0; k0 < K; k0 += BK) {
-            const bool more = k0 + BK < K;
-            if (more)
-                load_tile(k0 + BK);
+        // One K tile multiplied from shared buffer `buf`.
+        auto multiply = [&](int buf) {
 #pragma unroll
             for (int k = 0; k < BK; ++k) {
-                const float4 a0 = *reinterpret_cast<const float4*>(&As[k][4 * ty]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&As[k][64 + 4 * ty]);
-                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[k][4 * tx]);
-                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[k][64 + 4 * tx]);
+                const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * ty]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][64 + 4 * ty]);
+                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][4 * tx]);
+                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][64 + 4 * tx]);
                 const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
                 const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -294,10 +295,58 @@ __global__ void __launch_bounds__(256, 2)
                     for (int j = 0; j < 8; ++j)
                         acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
             }
-            __syncthreads();
-            if (more) {
-                store_tile();
+        };
+
+        // K tile t is multiplied from buffer t & 1, with one barrier per K
+        // tile.  The previous output tile's last barrier follows all of its
+        // shared-memory reads, so both buffers are free here.  Two schedules
+        // of the register prefetch, chosen per operand layout by measurement
+        // (FP32 4096^3 on GB300: one tile ahead 48.5 / 46.6 / 48.8 TFLOP/s
+        // for A, B as stored / B transposed / both transposed, two tiles
+        // ahead 45.3 against 40.3 for A transposed with B as stored):
+        //  - one ahead: tile t + 1 is loaded before the multiplies of tile t
+        //    and stored into the other buffer after them;
+        //  - two ahead: tile t + 1, loaded during iteration t - 1, is stored
+        //    first, then the loads of tile t + 2 are issued before the
+        //    multiplies, so a barrier lies between each load and its store.
+        set_tile(m0, n0);
+        if constexpr (OP_A && !OP_B) {
+            // two ahead
+            const int nk = (K + BK - 1) / BK;
+            if (nk > 0) {
+                load_tile(0);
+                store_tile(0);
+                if (nk > 1)
+                    load_tile(BK);
                 __syncthreads();
+            }
+            for (int t = 0; t < nk; ++t) {
+                const int buf = t & 1;
+                if (t + 1 < nk)
+                    store_tile(buf ^ 1);
+                if (t + 2 < nk)
+                    load_tile((t + 2) * BK);
+                multiply(buf);
+                __syncthreads();
+            }
+        } else {
+            // one ahead
+            int buf = 0;
+            if (K > 0) {
+                load_tile(0);
+                store_tile(0);
+                __syncthreads();
+            }
+            for (int k0 = 0; k0 < K; k0 += BK) {
+                const bool more = k0 + BK < K;
+                if (more)
+                    load_tile(k0 + BK);
+                multiply(buf);
+                // the other buffer was last read before the previous barrier
+                if (more)
+                    store_tile(buf ^ 1);
+                __syncthreads();
+                buf ^= 1;
             }
         }
 
@@ -330,9 +379,21 @@ cudaError_t launch_simt(const SimtLaunch& l, cudaStream_t stream)
         const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 2;
         const int grid = static_cast<int>(std::max<long long>(1, std::min(big_tiles, cap)));
         note_launch();
-        simt_gemm_big_kernel<InT, OutT><<<grid, 256, 0, stream>>>(
-            static_cast<const InT*>(l.A), static_cast<const InT*>(l.B), static_cast<OutT*>(l.C),
-            l.M, l.N, l.K, l.op_a, l.op_b, l.alpha, l.beta);
+        const InT* A = static_cast<const InT*>(l.A);
+        const InT* B = static_cast<const InT*>(l.B);
+        OutT* C = static_cast<OutT*>(l.C);
+        if (!l.op_a && !l.op_b)
+            simt_gemm_big_kernel<InT, OutT, false, false>
+                <<<grid, 256, 0, stream>>>(A, B, C, l.M, l.N, l.K, l.alpha, l.beta);
+        else if (l.op_a && !l.op_b)
+            simt_gemm_big_kernel<InT, OutT, true, false>
+                <<<grid, 256, 0, stream>>>(A, B, C, l.M, l.N, l.K, l.alpha, l.beta);
+        else if (!l.op_a && l.op_b)
+            simt_gemm_big_kernel<InT, OutT, false, true>
+                <<<grid, 256, 0, stream>>>(A, B, C, l.M, l.N, l.K, l.alpha, l.beta);
+        else
+            simt_gemm_big_kernel<InT, OutT, true, true>
+                <<<grid, 256, 0, stream>>>(A, B, C, l.M, l.N, l.K, l.alpha, l.beta);
         return cudaGetLastError();
     }
     const long long tiles = static_cast<long long>((l.M + BM - 1) / BM) * ((l.N + BN - 1) / BN);
