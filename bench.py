@@ -63,6 +63,9 @@ def parse_args():
                     help="instead of the benchmark line: time the extended forms (transposed "
                          "operands, alpha/beta, split-K, last-wave split) on fixed BF16 "
                          "problems, one JSON line each")
+    ap.add_argument("--simt", action="store_true",
+                    help="instead of the benchmark line: time the SIMT kernel on FP32 and "
+                         "unaligned 16-bit products in every operand layout, one JSON line each")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the GEMM launches (no e2e, cuBLAS context or CPU "
                          "baseline); used for profiler captures")
@@ -528,6 +531,21 @@ SWEEP_SHAPES = [(n, n, n) for n in (2048, 3072, 4096, 6144, 8192)] + [
     (12288, 12288, 2048), (1536, 1536, 1536), (2560, 2560, 2560), (5120, 5120, 1024)]
 
 
+def median_call_ms(f, steps):
+    """Median CUDA-event time in ms of one call of f, after 5 untimed calls."""
+    import torch
+    for _ in range(5):
+        f()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
+        f()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    return statistics.median([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
+
+
 def run_sweep():
     """Median per-call TFLOP/s of each tensor-core variant, the automatic
     choice and cuBLAS (torch.matmul) on BF16 inputs, BF16 output."""
@@ -536,17 +554,7 @@ def run_sweep():
     tg.load_library(build_if_missing=True)
     torch.cuda.set_device(0)
 
-    def timeit(f, steps):
-        for _ in range(5):
-            f()
-        torch.cuda.synchronize()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-        ev[0].record()
-        for i in range(steps):
-            f()
-            ev[i + 1].record()
-        torch.cuda.synchronize()
-        return statistics.median([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
+    timeit = median_call_ms
 
     g = torch.Generator(device="cuda").manual_seed(0)
     for M, N, K in SWEEP_SHAPES:
@@ -565,6 +573,48 @@ def run_sweep():
         print(json.dumps(row), flush=True)
 
 
+SIMT_SHAPES = [("f32", 4096, 4096, 4096), ("f32", 8192, 8192, 1024), ("f32", 2048, 2048, 2048),
+               ("bf16", 4095, 4095, 4095)]
+
+
+def run_simt():
+    """Median per-call TFLOP/s of the SIMT kernel (forced) on FP32 inputs and
+    on 16-bit inputs whose odd row pitch keeps them off the tensor cores, in
+    every operand layout, FP32 output; cuBLAS FP32 (TF32 off) beside the
+    row-major FP32 products, and the FP32 FMA peak at the maximum SM clock
+    (152 SMs x 128 lanes x 2 FLOP x 2.07 GHz) for scale.  A last line gives
+    the SM clocks sampled over the run."""
+    import torch
+    import tiled_matrix_multiplication_output_gb300 as tg
+    tg.load_library(build_if_missing=True)
+    torch.cuda.set_device(0)
+    torch.backends.cuda.matmul.allow_tf32 = False
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    fma_peak = sms * 128 * 2 * 2.07e9 / 1e12
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16}
+    g = torch.Generator(device="cuda").manual_seed(0)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    for name, M, N, K in SIMT_SHAPES:
+        flops = 2.0 * M * N * K
+        steps = max(10, min(100, int(2e11 / flops)))
+        for op_a, op_b in (("n", "n"), ("t", "n"), ("n", "t"), ("t", "t")):
+            A = torch.randn((K, M) if op_a == "t" else (M, K), device="cuda", generator=g).to(dt[name])
+            B = torch.randn((N, K) if op_b == "t" else (K, N), device="cuda", generator=g).to(dt[name])
+            C = torch.empty((M, N), device="cuda", dtype=torch.float32)
+            ms = median_call_ms(lambda: tg.addmm(A, B, C, op_a=op_a, op_b=op_b, kernel="simt"),
+                                steps)
+            row = {"in_dtype": name, "shape": [M, N, K], "layout": op_a + op_b,
+                   "us": round(ms * 1e3, 1), "tflops": round(flops / ms / 1e9, 2),
+                   "fma_peak_tflops_at_max_clock": round(fma_peak, 1)}
+            if name == "f32" and op_a == "n" and op_b == "n":
+                cb = median_call_ms(lambda: torch.matmul(A, B, out=C), steps)
+                row["cublas_f32_tflops"] = round(flops / cb / 1e9, 2)
+            print(json.dumps(row), flush=True)
+            del A, B, C
+    print(json.dumps({"clocks": clocks.stop()}), flush=True)
+
+
 def run_rows():
     """Median per-call time and TFLOP/s of the extended entry points."""
     import torch
@@ -572,17 +622,7 @@ def run_rows():
     tg.load_library(build_if_missing=True)
     torch.cuda.set_device(0)
 
-    def timeit(f, steps):
-        for _ in range(5):
-            f()
-        torch.cuda.synchronize()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-        ev[0].record()
-        for i in range(steps):
-            f()
-            ev[i + 1].record()
-        torch.cuda.synchronize()
-        return statistics.median([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
+    timeit = median_call_ms
 
     def emit(row, M, N, K, ms, **extra):
         print(json.dumps({"row": row, "shape": [M, N, K], "us": round(ms * 1e3, 2),
@@ -647,6 +687,9 @@ def main():
         return
     if args.rows:
         run_rows()
+        return
+    if args.simt:
+        run_simt()
         return
     world_env = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
