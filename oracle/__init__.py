@@ -11,7 +11,9 @@ multiply and add separately rounded on both x86 and Arm hosts.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -38,17 +40,37 @@ _i64 = ctypes.c_int64
 _p = ctypes.c_void_p
 
 
+def _build_cmd(out: str) -> list[str]:
+    return ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+            "-pthread", "-Wall", "-Wextra", "-o", out, _SRC, "-lm"]
+
+
+def _stamp() -> str:
+    """SHA-256 of the source, the compiler command and the host architecture."""
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(_build_cmd("<out>")).replace(_HERE, "<oracle>").encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile oracle.c into a shared library; returns its path."""
+    """Compile oracle.c into a shared library unless the one on disk was
+    built from this source with this command; returns its path."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
+    stamp = _stamp()
+    stamp_path = _LIB_PATH + ".sha256"
+    if not force and os.path.exists(_LIB_PATH) and os.path.exists(stamp_path):
+        with open(stamp_path) as f:
+            if f.read().strip() == stamp:
+                return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-           "-pthread", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    subprocess.run(_build_cmd(tmp), check=True)
     os.replace(tmp, _LIB_PATH)
+    with open(stamp_path + f".{os.getpid()}", "w") as f:
+        f.write(stamp + "\n")
+    os.replace(stamp_path + f".{os.getpid()}", stamp_path)
     return _LIB_PATH
 
 
