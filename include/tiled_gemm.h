@@ -40,6 +40,12 @@
 extern "C" {
 #endif
 
+/* The largest M, N or K any entry point accepts: 2^31 - 256.  Sizes stay
+   below 2^31 with a tile's worth of headroom, so that every index a kernel
+   forms (a tile's first row plus its extent, a K offset plus one K tile)
+   fits a 32-bit signed integer. */
+#define GEMM_MAX_DIM ((int64_t)2147483392)
+
 /* Storage / arithmetic types. */
 typedef enum {
     GEMM_F32 = 0,  /* IEEE binary32 */
@@ -49,8 +55,8 @@ typedef enum {
 
 typedef enum {
     GEMM_OK = 0,
-    GEMM_ERR_INVALID_VALUE = 1, /* null pointer where data is needed, negative or >= 2^31 size,
-                                   unknown enum value */
+    GEMM_ERR_INVALID_VALUE = 1, /* null pointer where data is needed, negative size or one
+                                   above GEMM_MAX_DIM, unknown enum value */
     GEMM_ERR_UNSUPPORTED = 2,   /* valid but unsupported combination (types, or a forced
                                    kernel whose alignment rules the operands break) */
     GEMM_ERR_CUDA = 3,          /* a CUDA runtime call or the launch failed */
@@ -87,7 +93,7 @@ typedef enum {
  * accumulator is initialised to zero and no K tile is added).
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_VALUE (a null A or B with K > 0 and
- * M*N > 0, a null C with M*N > 0, a negative size or one >= 2^31, an unknown
+ * M*N > 0, a null C with M*N > 0, a negative size or one above GEMM_MAX_DIM, an unknown
  * dtype), GEMM_ERR_UNSUPPORTED (another type combination) or GEMM_ERR_CUDA.
  */
 int gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
@@ -289,6 +295,28 @@ int gemm_select_kernel(const void* A, const void* B, const void* C, int64_t M, i
 int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M, int64_t N,
                  int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
                  gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* stream);
+
+/*
+ * gemm_ex_host_ws -- gemm_ex_host whose products (the whole product, or each
+ * row panel's) run as gemm_ex_ws with the caller's device workspace:
+ * the tiles of a panel's last, partial wave are split along K across the
+ * idle CTA pairs, as on the device path.  workspace may be NULL (then this
+ * is gemm_ex_host); otherwise it must be 16-byte aligned, and
+ * gemm_workspace_size(M, N, K) bytes always suffice.  The panels run one
+ * after another on `stream` and share the workspace.  Errors as
+ * gemm_ex_ws.
+ */
+int gemm_ex_host_ws(const void* A_host, const void* B_host, void* C_host, int64_t M, int64_t N,
+                    int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                    gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * gemm_host_panel_rows -- the rows of A and C in one panel of the pipelined
+ * host-buffer path for an M-row product with K > 0 (M itself when the
+ * product runs as one piece); 0 for M <= 0 or M > GEMM_MAX_DIM.
+ */
+int64_t gemm_host_panel_rows(int64_t M);
 
 /*
  * gemm_device_status -- synchronize `stream`, then read and clear the status

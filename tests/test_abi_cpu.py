@@ -37,6 +37,19 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert tg.gemm(p, p, p, 4, -1, 4, tg.BF16, tg.F32) == INV
     assert tg.gemm(p, p, p, 4, 4, -1, tg.BF16, tg.F32) == INV
     assert tg.gemm(p, p, p, 1 << 31, 4, 4, tg.BF16, tg.F32) == INV
+    # the size limit: 2^31 - 256, so that a tile's or a K tile's worth of
+    # headroom above any accepted size still fits a 32-bit index
+    big = (1 << 31) - 256
+    assert tg.binding.MAX_DIM == big
+    for dims in ((big + 1, 4, 4), (4, big + 1, 4), (4, 4, big + 1), ((1 << 31) - 1, 4, 4)):
+        assert tg.gemm(p, p, p, *dims, tg.BF16, tg.F32) == INV, dims
+        assert tg.gemm_general(p, p, p, *dims, 0, 0, 1.0, 0.0, tg.F32, tg.F32, tg.F32, 1,
+                               None) == INV, dims
+        assert tg.gemm_ex_ws(p, p, p, *dims, tg.BF16, tg.F32, tg.F32, None, 0, None) == INV
+        assert tg.gemm_splitk_noalloc(p, p, p, *dims, 2, tg.BF16, tg.F32, tg.F32, None) == INV
+    # at the limit itself a size is accepted (an empty product: nothing launches)
+    assert tg.gemm(p, p, p, big, 0, 4, tg.BF16, tg.F32) == 0
+    assert tg.gemm(p, p, p, 0, big, big, tg.BF16, tg.F32) == 0
     assert tg.gemm(p, p, None, 4, 4, 4, tg.BF16, tg.F32) == INV       # null C
     assert tg.gemm(None, p, p, 4, 4, 4, tg.BF16, tg.F32) == INV       # null A with K > 0
     assert tg.gemm(p, p, p, 4, 4, 4, 7, tg.F32) == INV                # unknown dtype
@@ -90,3 +103,22 @@ def test_library_traffic_model_matches_oracle_walker(lib):
 def test_library_traffic_model_rejects_bad_tiles(lib):
     with pytest.raises(tg.GemmError):
         tg.gemm_traffic_model(8, 8, 8, 0, 8, 8)
+
+
+def test_host_panel_rows(lib):
+    # whole 256-row tile rows, about an eighth of M, at least 1024; one piece
+    # when that leaves a single panel
+    assert tg.gemm_host_panel_rows(8192) == 1024
+    assert tg.gemm_host_panel_rows(4100) == 1024
+    assert tg.gemm_host_panel_rows(20000) == 2560
+    assert tg.gemm_host_panel_rows(1000) == 1000
+    assert tg.gemm_host_panel_rows(1024) == 1024
+    assert tg.gemm_host_panel_rows(0) == 0
+    assert tg.gemm_host_panel_rows(-5) == 0
+    assert tg.gemm_host_panel_rows(tg.binding.MAX_DIM + 1) == 0
+
+
+def test_header_constants_match_the_binding():
+    text = open(tg.binding.HEADER).read()
+    assert "#define GEMM_MAX_DIM ((int64_t)2147483392)" in text
+    assert 2147483392 == tg.binding.MAX_DIM

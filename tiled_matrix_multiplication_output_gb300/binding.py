@@ -23,6 +23,9 @@ DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16}
 
 OK, ERR_INVALID_VALUE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 
+# The largest M, N or K the library accepts (GEMM_MAX_DIM).
+MAX_DIM = (1 << 31) - 256
+
 KERNELS = {
     "auto": 0,
     "simt": 1,
@@ -52,6 +55,9 @@ _SIGNATURES = {
     "gemm_general": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, ctypes.c_float, ctypes.c_float,
                       _int, _int, _int, _int, _p], _int),
     "gemm_ex_host": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, _p, _p, _p], _int),
+    "gemm_ex_host_ws": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, _p, _p, _p,
+                         ctypes.c_size_t, _p], _int),
+    "gemm_host_panel_rows": ([_i64], _i64),
     "gemm_workspace_size": ([_i64, _i64, _i64], ctypes.c_size_t),
     "gemm_ex_ws": ([_p, _p, _p, _i64, _i64, _i64, _int, _int, _int, _p, ctypes.c_size_t, _p],
                    _int),
@@ -133,6 +139,17 @@ def gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype
                  stream=None) -> int:
     return load_library().gemm_ex_host(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype,
                                        out_dtype, dA, dB, dC, stream)
+
+
+def gemm_ex_host_ws(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype, dA, dB, dC,
+                    workspace, workspace_bytes, stream=None) -> int:
+    return load_library().gemm_ex_host_ws(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype,
+                                          out_dtype, dA, dB, dC, workspace, workspace_bytes,
+                                          stream)
+
+
+def gemm_host_panel_rows(M) -> int:
+    return load_library().gemm_host_panel_rows(M)
 
 
 def gemm_workspace_size(M, N, K) -> int:

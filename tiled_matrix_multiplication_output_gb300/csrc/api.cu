@@ -68,8 +68,7 @@ int validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, 
 {
     if (!valid_dtype(in_dtype) || !valid_dtype(acc_dtype) || !valid_dtype(out_dtype))
         return GEMM_ERR_INVALID_VALUE;
-    const int64_t lim = int64_t(1) << 31;
-    if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim)
+    if (M < 0 || N < 0 || K < 0 || M > GEMM_MAX_DIM || N > GEMM_MAX_DIM || K > GEMM_MAX_DIM)
         return GEMM_ERR_INVALID_VALUE;
     if (M > 0 && N > 0) {
         if (!C)
@@ -491,9 +490,29 @@ cudaError_t host_pipe(HostPipe** out)
 }  // namespace
 }  // namespace tmmo
 
-extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
-                            int64_t N, int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
-                            gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* stream)
+namespace tmmo {
+namespace {
+
+// Rows per panel of the pipelined host-buffer path: whole 256-row tile rows,
+// about an eighth of M, at least 1024.  Eight panels rather than four
+// shorten the last copy-compute-copy chain: 1.65 vs 1.74 ms for 8192^3 BF16
+// on GB300 (host links at about 210 GB/s each way).
+#ifndef TMMO_HOST_PANELS
+#define TMMO_HOST_PANELS 8
+#endif
+int64_t host_panel_rows(int64_t M)
+{
+    int64_t panel = ((M + TMMO_HOST_PANELS - 1) / TMMO_HOST_PANELS + 255) / 256 * 256;
+    return panel < 1024 ? 1024 : panel;
+}
+
+// The host-buffer path.  Each product (the whole one, or one panel's) goes
+// through gemm_ex_ws, so with a workspace it gets the last-wave and few-tile
+// splits of the device path; without one it is plain gemm_ex.
+int host_pipeline(const void* A_host, const void* B_host, void* C_host, int64_t M, int64_t N,
+                  int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                  gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* workspace,
+                  size_t workspace_bytes, void* stream)
 {
     int rc = validate(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype);
     if (rc != GEMM_OK)
@@ -503,22 +522,18 @@ extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host
         return rc;
     if (M == 0 || N == 0)
         return GEMM_OK;
+    if (workspace && !aligned16(workspace))
+        return GEMM_ERR_INVALID_VALUE;
+    if (!workspace)
+        workspace_bytes = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t in_b = static_cast<size_t>(dt_size(in_dtype));
     const size_t out_b = static_cast<size_t>(dt_size(out_dtype));
     const size_t a_row = size_t(K) * in_b, c_row = size_t(N) * out_b;
     // Row panels of A and C: B is copied once, then the copy of A's panel
-    // i + 1 and of C's panel i - 1 overlap the product of panel i.  Panels
-    // are whole 256-row tile rows, at least 1024 rows; small products (or
-    // K == 0) run as one panel on the caller's stream.  Eight panels rather
-    // than four shorten the last copy-compute-copy chain: 1.65 vs 1.74 ms for
-    // 8192^3 BF16 on GB300 (host links at about 210 GB/s each way).
-#ifndef TMMO_HOST_PANELS
-#define TMMO_HOST_PANELS 8
-#endif
-    int64_t panel = ((M + TMMO_HOST_PANELS - 1) / TMMO_HOST_PANELS + 255) / 256 * 256;
-    if (panel < 1024)
-        panel = 1024;
+    // i + 1 and of C's panel i - 1 overlap the product of panel i.  Small
+    // products (or K == 0) run as one panel on the caller's stream.
+    const int64_t panel = host_panel_rows(M);
     const int64_t panels = (M + panel - 1) / panel;
     if (K == 0 || panels <= 1 || panels > kMaxPanels) {
         if (K > 0) {
@@ -528,7 +543,8 @@ extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host
                                 s) != cudaSuccess)
                 return GEMM_ERR_CUDA;
         }
-        rc = run(plain(dA, dB, dC, M, N, K, in_dtype, acc_dtype, out_dtype), GEMM_KERNEL_AUTO, s);
+        rc = gemm_ex_ws(dA, dB, dC, M, N, K, in_dtype, acc_dtype, out_dtype, workspace,
+                        workspace_bytes, stream);
         if (rc != GEMM_OK)
             return rc;
         if (cudaMemcpyAsync(C_host, dC, size_t(M) * c_row, cudaMemcpyDeviceToHost, s) != cudaSuccess)
@@ -559,8 +575,8 @@ extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host
             !ok(cudaEventRecord(h->a_done[i], h->in)) ||
             !ok(cudaStreamWaitEvent(s, h->a_done[i], 0)))
             return GEMM_ERR_CUDA;
-        rc = run(plain(a_dst, dB, c_dev, rows, N, K, in_dtype, acc_dtype, out_dtype),
-                 GEMM_KERNEL_AUTO, s);
+        rc = gemm_ex_ws(a_dst, dB, c_dev, rows, N, K, in_dtype, acc_dtype, out_dtype, workspace,
+                        workspace_bytes, stream);
         if (rc != GEMM_OK)
             return rc;
         if (!ok(cudaEventRecord(h->c_done[i], s)) || !ok(cudaStreamWaitEvent(h->out, h->c_done[i], 0)) ||
@@ -571,6 +587,35 @@ extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host
     if (!ok(cudaEventRecord(h->done, h->out)) || !ok(cudaStreamWaitEvent(s, h->done, 0)))
         return GEMM_ERR_CUDA;
     return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace tmmo
+
+extern "C" int gemm_ex_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
+                            int64_t N, int64_t K, gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype,
+                            gemm_dtype_t out_dtype, void* dA, void* dB, void* dC, void* stream)
+{
+    return host_pipeline(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype, dA, dB,
+                         dC, nullptr, 0, stream);
+}
+
+extern "C" int gemm_ex_host_ws(const void* A_host, const void* B_host, void* C_host, int64_t M,
+                               int64_t N, int64_t K, gemm_dtype_t in_dtype,
+                               gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype, void* dA, void* dB,
+                               void* dC, void* workspace, size_t workspace_bytes, void* stream)
+{
+    return host_pipeline(A_host, B_host, C_host, M, N, K, in_dtype, acc_dtype, out_dtype, dA, dB,
+                         dC, workspace, workspace_bytes, stream);
+}
+
+extern "C" int64_t gemm_host_panel_rows(int64_t M)
+{
+    if (M <= 0 || M > GEMM_MAX_DIM)
+        return 0;
+    const int64_t panel = host_panel_rows(M);
+    const int64_t panels = (M + panel - 1) / panel;
+    return (panels <= 1 || panels > kMaxPanels) ? M : panel;
 }
 
 extern "C" int gemm_device_status(void* stream)
