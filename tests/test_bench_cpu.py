@@ -141,3 +141,23 @@ def test_roofline_fp32_compute_bound_is_the_fma_pipes():
     r = bench.roofline_of(w, _flops(w), 3.0, PEAKS, "measured", None)
     assert r["bound"] == "alu"
     assert r["peak"] == pytest.approx(152 * 128 * 2 * 2070e6 / 1e12)
+
+
+def test_roofline_carries_the_theoretical_tensor_peak():
+    # 152 SMs x 8192 dense FLOP per cycle x 2070 MHz = 2577.7 TFLOP/s; at a
+    # sampled 1485 MHz under the power cap, 1849.3
+    w = inputs.WORKLOADS["square_8192_bf16"]
+    r = bench.roofline_of(w, _flops(w), 0.6, PEAKS, "measured", None, sms=152, run_mhz=1485.0)
+    assert r["theoretical_peak"] == pytest.approx(152 * 8192 * 2070e6 / 1e12)
+    assert r["frac_of_theoretical"] == pytest.approx(r["achieved"] / r["theoretical_peak"])
+    assert r["theoretical_peak_at_run_clock"] == pytest.approx(152 * 8192 * 1485e6 / 1e12)
+    assert r["frac_of_theoretical_at_run_clock"] == pytest.approx(
+        r["achieved"] / r["theoretical_peak_at_run_clock"])
+    # the measured cuBLAS burst lies below the theoretical peak
+    assert PEAKS["bf16_tflops"] < r["theoretical_peak"]
+    # no sampled clock: no run-clock fraction; HBM-bound lines carry none of it
+    assert "frac_of_theoretical_at_run_clock" not in bench.roofline_of(
+        w, _flops(w), 0.6, PEAKS, "measured", None)
+    small = inputs.WORKLOADS["square_128_f16"]
+    assert "theoretical_peak" not in bench.roofline_of(small, _flops(small), 0.01, PEAKS,
+                                                        "measured", None)

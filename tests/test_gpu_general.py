@@ -55,8 +55,7 @@ def test_transposes_random_tolerance(op_a, op_b):
     ref, Cabs = oracle.gemm_general(A, B, op_a, op_b)
     for kernel in TC_KERNELS + ("simt",):
         for out in (torch.float32, torch.bfloat16):
-            tolerance_check(_run(A, B, op_a, op_b, kernel, out_dtype=out), ref, Cabs,
-                            with_output_rounding=(out != torch.float32))
+            tolerance_check(_run(A, B, op_a, op_b, kernel, out_dtype=out), ref, Cabs)
 
 
 @pytest.mark.parametrize("kernel", TC_KERNELS + ("simt", "simt_tpb3"))

@@ -2,6 +2,8 @@
 inputs: bit-exact on integer-valued inputs, within the stated tolerance on
 random FP16/BF16/FP32 inputs, on every kernel, at sizes spanning several
 tiles with ragged tails in M, N and K."""
+import itertools
+
 import numpy as np
 import pytest
 import torch
@@ -9,7 +11,8 @@ import torch
 import oracle
 import tiled_matrix_multiplication_output_gb300 as tg
 from tests.conftest import load_worked_9x9
-from tests.helpers import ALL_KERNELS, TC_KERNELS, expect_close, expect_exact, run_gpu
+from tests.helpers import (ALL_KERNELS, TC_KERNELS, expect_close, expect_exact, run_gpu,
+                           tolerance_check)
 from tiled_matrix_multiplication_output_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -70,24 +73,73 @@ def test_simt_ragged_exact(kernel, in_dtype):
 
 # ------------------------------------------------- brute force, tiny shapes
 
-def test_brute_force_tiny_shapes_all_kernels():
-    """M, N in 1..17 and K in 1..17 sampled (plus a few tile edges), integer
-    inputs: every kernel that accepts the shape is bit-exact."""
+def _exact_cases(cases, kernels):
+    """Each (M, N, K, in_dtype, out_dtype, seed) case on each kernel, all
+    launched before one synchronisation, then compared bit for bit with the
+    oracle's exact integer product rounded to the output type."""
+    runs = []
+    for M, N, K, in_dt, out_dt, seed in cases:
+        A, B = inputs.draw(M, N, K, in_dt, "int", seed=seed)
+        dA, dB = A.cuda(), B.cuda()
+        outs = [(k, tg.matmul(dA, dB, out_dtype=out_dt, kernel=k)) for k in kernels]
+        runs.append((A, B, outs))
+    assert tg.gemm_device_status(torch.cuda.current_stream().cuda_stream) == tg.binding.OK
+    for A, B, outs in runs:
+        C_ref, _ = oracle.gemm(A, B, nthreads=1)
+        for kernel, C in outs:
+            want = oracle.round_to(C_ref, C.dtype).double().numpy()
+            got = C.cpu().double().numpy()
+            if not np.array_equal(got, want):
+                raise AssertionError(f"{kernel} not exact at M, N, K = {tuple(A.shape) + (B.shape[1],)}")
+
+
+OUT_CYCLE = (torch.float32, torch.float16, torch.bfloat16)
+
+
+def test_brute_force_every_tiny_shape_simt():
+    """Every (M, N, K) in {1..17}^3 (4913 shapes) on both SIMT kernels,
+    integer inputs in [-4, 4]: bit-exact.  The input type cycles F32, F16,
+    BF16 and the output type F32, F16, BF16 (offset), so every pair occurs."""
+    in_cycle = ("f32", "f16", "bf16")
+    cases = [(M, N, K, in_cycle[i % 3], OUT_CYCLE[(i // 3) % 3], i)
+             for i, (M, N, K) in enumerate(itertools.product(range(1, 18), repeat=3))]
+    for start in range(0, len(cases), 500):
+        _exact_cases(cases[start:start + 500], ("simt", "simt_tpb3"))
+
+
+def test_brute_force_every_tiny_shape_tensor_cores():
+    """Every (M, 8n, 8k) in the {1..17}^3 cube -- M in 1..17, N and K in
+    {8, 16}, the sizes whose 16-bit rows meet the 16-byte TMA rule -- on
+    every tensor-core kernel, FP16 and BF16 inputs, every output type."""
+    cases = [(M, N, K, "f16" if i % 2 else "bf16", OUT_CYCLE[i % 3], 5000 + i)
+             for i, (M, N, K) in enumerate(itertools.product(range(1, 18), (8, 16), (8, 16)))]
+    _exact_cases(cases, TC_KERNELS)
+
+
+def test_brute_force_tile_edges_all_kernels():
+    """Dimensions one below and one above a 64- and a 128-wide tile
+    (63, 65, 127, 129) against tiny ones, on every kernel that accepts them:
+    SIMT for any size, tensor cores for N and K multiples of 8."""
+    dims = (1, 17, 63, 65, 127, 129)
+    simt = [(M, N, K, "bf16", OUT_CYCLE[i % 3], 6000 + i)
+            for i, (M, N, K) in enumerate(itertools.product(dims, repeat=3)) if max(M, N, K) >= 63]
+    _exact_cases(simt, ("simt", "simt_tpb3"))
+    tc = [(M, N, K, "f16", OUT_CYCLE[i % 3], 7000 + i)
+          for i, (M, N, K) in enumerate(itertools.product(dims, (8, 64, 72, 136), (8, 56, 72, 136)))]
+    _exact_cases(tc, TC_KERNELS)
+
+
+def test_random_tensor_core_shapes_exact():
+    """24 seeded random shapes up to 300 x 320 x 320 on every tensor-core
+    kernel, integer inputs: bit-exact."""
     rng = np.random.default_rng(5)
-    dims = list(range(1, 18)) + [63, 64, 65, 127, 128, 129]
-    for trial in range(40):
-        M, N, K = (int(rng.choice(dims)) for _ in range(3))
-        A, B = inputs.draw(M, N, K, "bf16", "int", seed=trial)
-        for kernel in ("simt", "simt_tpb3"):
-            expect_exact(run_gpu(A, B, torch.float32, kernel), A, B)
-    # tensor-core kernels need N and K multiples of 8 (16-byte rows)
+    cases = []
     for trial in range(24):
         M = int(rng.integers(1, 300))
         N = 8 * int(rng.integers(1, 40))
         K = 8 * int(rng.integers(1, 40))
-        A, B = inputs.draw(M, N, K, "f16", "int", seed=100 + trial)
-        for kernel in TC_KERNELS:
-            expect_exact(run_gpu(A, B, torch.float32, kernel), A, B)
+        cases.append((M, N, K, "f16", torch.float32, 100 + trial))
+    _exact_cases(cases, TC_KERNELS)
 
 
 # ----------------------------------------------- random values, tolerance
@@ -103,14 +155,28 @@ def test_random_bf16_within_tolerance(kernel):
 @pytest.mark.parametrize("kernel", ["simt", "auto"])
 def test_random_f32_within_tolerance(kernel):
     A, B = inputs.draw(257, 129, 515, "f32", "normal", seed=8)
-    expect_close(run_gpu(A, B, torch.float32, kernel), A, B, with_output_rounding=False)
+    expect_close(run_gpu(A, B, torch.float32, kernel), A, B)
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_same_sign_products(kernel):
+    """Inputs on U[0, 1]: every product positive, so |C_ref| = sum|ab|.  FP32
+    and FP16 outputs meet the stated bound as it is; a BF16 output gets half
+    an ulp of BF16 on top, because its final rounding alone (2^-9 |C|)
+    exceeds 1e-3 sum|ab| when nothing cancels."""
+    M, N, K = (200, 136, 1000) if kernel != "simt_tpb3" else (40, 24, 300)
+    A, B = inputs.draw(M, N, K, "bf16", "positive", seed=16)
+    C_ref, Cabs = oracle.gemm(A, B)
+    for out in (torch.float32, torch.float16):
+        tolerance_check(run_gpu(A, B, out, kernel), C_ref, Cabs)
+    tolerance_check(run_gpu(A, B, torch.bfloat16, kernel), C_ref, Cabs, same_sign=True)
 
 
 @pytest.mark.parametrize("kernel", TC_KERNELS)
 def test_large_k_and_many_tiles(kernel):
     """K = 4104 (64 K steps + a ragged 8) and a 3 x 5 grid of tiles."""
     A, B = inputs.draw(520, 1160, 4104, "f16", "uniform", seed=9)
-    expect_close(run_gpu(A, B, torch.float32, kernel), A, B, with_output_rounding=False)
+    expect_close(run_gpu(A, B, torch.float32, kernel), A, B)
 
 
 # ---------------------------------------------------------- special cases
@@ -199,7 +265,7 @@ def test_stream_ordering_on_side_stream():
         C = tg.matmul(dA, dB, out_dtype=torch.float32)
         Ch = C.cpu()
     s.synchronize()
-    expect_close(Ch, A, B, with_output_rounding=False)
+    expect_close(Ch, A, B)
 
 
 def test_host_buffer_entry_point_pipelined():
@@ -227,6 +293,50 @@ def test_host_buffer_entry_point_pipelined():
         expect_exact(C, A, B)
     # work queued after the call on the same stream sees the finished product
     assert torch.equal(dC.cpu(), outs[-1][2])
+
+
+@pytest.mark.parametrize("M, N, K, out_dtype", [
+    (4100, 520, 264, torch.float32),     # 5 panels of 1024 rows, the last one 4 rows
+    (8192, 2048, 776, torch.bfloat16),   # 8 panels of 1024 rows: 32 pair tiles each, one
+                                         # partial wave split along K in every panel
+    (700, 4096, 1024, torch.float16),    # a single piece
+])
+def test_host_buffer_entry_point_with_workspace(M, N, K, out_dtype):
+    """gemm_ex_host_ws: each panel's product through the workspace path
+    (last-wave split); exact on integer inputs, as gemm_ex_host is, and within
+    the stated bound on random inputs."""
+    s = torch.cuda.current_stream()
+    dA = torch.empty(M, K, dtype=torch.float16, device="cuda")
+    dB = torch.empty(K, N, dtype=torch.float16, device="cuda")
+    dC = torch.empty(M, N, dtype=out_dtype, device="cuda")
+    ws_bytes = tg.gemm_workspace_size(M, N, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    code = tg.binding.dtype_code(out_dtype)
+    for dist in ("int", "normal"):
+        A, B = inputs.draw(M, N, K, "f16", dist, seed=34)
+        Ah, Bh = A.pin_memory(), B.pin_memory()
+        C_ws = torch.empty(M, N, dtype=out_dtype).pin_memory()
+        C_plain = torch.empty(M, N, dtype=out_dtype).pin_memory()
+        rc = tg.gemm_ex_host_ws(Ah.data_ptr(), Bh.data_ptr(), C_ws.data_ptr(), M, N, K, tg.F16,
+                                tg.F32, code, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                                ws.data_ptr(), ws_bytes, s.cuda_stream)
+        assert rc == 0
+        s.synchronize()
+        rc = tg.gemm_ex_host(Ah.data_ptr(), Bh.data_ptr(), C_plain.data_ptr(), M, N, K, tg.F16,
+                             tg.F32, code, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                             s.cuda_stream)
+        assert rc == 0
+        assert tg.gemm_device_status(s.cuda_stream) == 0
+        if dist == "int":
+            expect_exact(C_ws, A, B)
+            expect_exact(C_plain, A, B)
+        else:
+            expect_close(C_ws, A, B)
+    # a misaligned workspace is refused before anything is queued
+    assert tg.gemm_ex_host_ws(Ah.data_ptr(), Bh.data_ptr(), C_ws.data_ptr(), M, N, K, tg.F16,
+                              tg.F32, code, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                              ws.data_ptr() + 4, ws_bytes - 4, s.cuda_stream) == \
+        tg.binding.ERR_INVALID_VALUE
 
 
 def test_automatic_choice_on_the_named_workloads():
@@ -291,3 +401,100 @@ def test_simt_large_tile_kernel_layouts_ragged_k_tiles(op_a, op_b):
                      kernel="simt").cpu()
         ref, _ = oracle.gemm_general(A, B, op_a, op_b)
         np.testing.assert_array_equal(C.double().numpy(), ref, err_msg=f"K={K} {in_dtype}")
+
+
+def test_simt_large_tile_kernel_more_tiles_than_blocks():
+    """More 128 x 128 tiles than the large-tile SIMT kernel has resident
+    blocks (2600^2: 21 x 21 = 441 tiles against two blocks per SM), so blocks
+    move on to a second output tile with their shared buffers and register
+    prefetch restarted: every operand layout, ragged in M, N and K (1, 3 and
+    10 K tiles of 8), integer inputs, exact against the oracle's general
+    form."""
+    M = N = 2600
+    assert 21 * 21 > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    for K, seed in ((5, 50), (21, 51), (77, 52)):
+        A0, B0 = inputs.draw(M, N, K, "f32", "int", seed=seed)
+        for op_a, op_b in (("n", "n"), ("t", "n"), ("n", "t"), ("t", "t")):
+            A = A0.t().contiguous() if op_a == "t" else A0
+            B = B0.t().contiguous() if op_b == "t" else B0
+            C = tg.addmm(A.cuda(), B.cuda(), op_a=op_a, op_b=op_b, out_dtype=torch.float32,
+                         kernel="simt").cpu()
+            ref, _ = oracle.gemm_general(A, B, op_a, op_b)
+            np.testing.assert_array_equal(C.double().numpy(), ref,
+                                          err_msg=f"K={K} layout {op_a}{op_b}")
+
+
+# ------------------------------------------------- IEEE special values
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_nan_and_inf_propagate(kernel):
+    """A NaN in A poisons its row of C; an infinity in A or B makes its row
+    or column infinite with the sign of each product, except where it meets
+    a zero (inf * 0 = NaN) or an infinity of the other sign (NaN).  Integer
+    values elsewhere keep every finite partial sum exact, so the class of
+    each result (finite value, +inf, -inf, NaN) does not depend on the
+    summation order, and each element must equal the oracle's FP64 IEEE
+    result rounded to the output type."""
+    M, N, K = (136, 200, 72) if kernel != "simt_tpb3" else (20, 24, 18)
+    for in_dt in ("f16", "bf16"):
+        A, B = inputs.draw(M, N, K, in_dt, "int", seed=70)
+        A[3, 5] = float("nan")
+        A[7, 2] = float("inf")
+        A[9, 4] = float("-inf")
+        B[4, 11] = float("-inf")
+        B[6, 13] = float("nan")
+        B[2, 17] = 0.0                   # A[7, 2] = inf meets a zero: NaN at (7, 17)
+        C_ref, _ = oracle.gemm(A, B)
+        for out in OUT_TYPES:
+            got = run_gpu(A, B, out, kernel).double().numpy()
+            want = oracle.round_to(C_ref, out).double().numpy()
+            assert np.isnan(want[3]).all() and np.isnan(want[:, 13]).all()
+            assert np.isnan(want[7, 17])
+            np.testing.assert_array_equal(got, want, err_msg=f"{in_dt} -> {out}")
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_f16_output_overflow_rounds_to_infinity(kernel):
+    """FP32 sums around the binary16 limit, written as FP16: 65504 stays,
+    65519 rounds down to 65504, 65520 (the midpoint to 65536) and beyond
+    become +-inf, as IEEE nearest-even rounding gives.  C[i, j] = 65504 s +
+    d with exact FP32 sums from an FP16 65504 and small integers."""
+    M, N, K = (40, 64, 16) if kernel != "simt_tpb3" else (8, 16, 16)
+    d = [0, 1, 15, 16, 17, 31, 32, 100, -16, -17, -1000, 0]
+    A = torch.zeros(M, K, dtype=torch.float16)
+    A[:, 0] = 1.0
+    A[:, 1] = 1.0
+    A[1::2, 0] = -1.0                          # odd rows: -65504 s + d
+    B = torch.zeros(K, N, dtype=torch.float16)
+    for j in range(N):
+        B[0, j] = 65504.0
+        B[1, j] = float(d[j % len(d)])
+    C_ref, _ = oracle.gemm(A, B)
+    want = oracle.round_to(C_ref, torch.float16)
+    assert torch.isinf(want).any() and (want.abs() == 65504).any()
+    got = run_gpu(A, B, torch.float16, kernel)
+    np.testing.assert_array_equal(got.double().numpy(), want.double().numpy())
+    # the FP32 and BF16 outputs of the same sums are finite and exact
+    for out in (torch.float32, torch.bfloat16):
+        np.testing.assert_array_equal(run_gpu(A, B, out, kernel).double().numpy(),
+                                      oracle.round_to(C_ref, out).double().numpy())
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_fp32_accumulator_overflow(kernel):
+    """Products beyond the FP32 range (2^100 * 2^100 in BF16 inputs) overflow
+    the FP32 accumulator to +-inf; the oracle's FP64 sum (2^200) rounds to
+    +-inf in every output type, so both sides agree element for element."""
+    M, N, K = (16, 32, 16) if kernel != "simt_tpb3" else (6, 8, 16)
+    A = torch.zeros(M, K, dtype=torch.bfloat16)
+    B = torch.zeros(K, N, dtype=torch.bfloat16)
+    A[:, 0] = 2.0 ** 100
+    A[::2, 0] = -(2.0 ** 100)
+    B[0, : N // 2] = 2.0 ** 100
+    B[1, :] = 3.0
+    A[:, 1] = 1.0
+    C_ref, _ = oracle.gemm(A, B)
+    for out in OUT_TYPES:
+        want = oracle.round_to(C_ref, out).double().numpy()
+        assert np.isinf(want[:, : N // 2]).all() and np.isfinite(want[:, N // 2:]).all()
+        np.testing.assert_array_equal(run_gpu(A, B, out, kernel).double().numpy(), want)

@@ -1,10 +1,13 @@
 """The five named workloads at their full sizes, through the C ABI in the
-launch configuration bench.py times (automatic kernel choice).
+launch configuration bench.py times (gemm_ex_ws with a workspace, automatic
+kernel choice) and through plain gemm_ex.
 
-Small workloads are compared with the oracle element by element; the 4096^3
-and 8192^3 products are compared on sampled outputs (every tile corner and
-edge plus random entries, each an oracle dot product) and by row and column
-sums, which involve every output element."""
+Every workload is compared with the oracle element by element over the
+whole output, at the stated bound |C - C_ref| <= 1e-3 sum|ab| + 1e-6 with
+nothing added: the 4096^3 and 8192^3 products too (the oracle, an FP64 loop
+over all host cores, takes about 7 s and 55 s for them on a 16-core host)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -12,7 +15,7 @@ import torch
 import oracle
 import tiled_matrix_multiplication_output_gb300 as tg
 from tests.conftest import load_golden
-from tests.helpers import HALF_ULP, expect_exact, run_gpu, sample_indices, tolerance_check
+from tests.helpers import expect_exact, run_gpu, sample_indices, tolerance_check
 from tiled_matrix_multiplication_output_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
@@ -42,7 +45,7 @@ def test_square_128_f16_and_traffic_model():
     A, B = inputs.make(w)
     C_ref, Cabs = oracle.gemm(A, B)
     for kernel in ("auto", "tc_128x128", "tc_128x256", "tc_256x256", "tc_256x128", "simt"):
-        tolerance_check(run_gpu(A, B, _out(w), kernel), C_ref, Cabs, with_output_rounding=False)
+        tolerance_check(run_gpu(A, B, _out(w), kernel), C_ref, Cabs)
     g = load_golden("page_figures.txt")
     t = oracle.traffic(128, 128, 128, 16, 16, 32, in_bytes=2, acc_bytes=4, c_bytes=4)
     assert t["bytes"] == int(g["traffic_128_tile16x16x32_total_kib"]) * 1024
@@ -54,61 +57,57 @@ def test_edge_96x200x1000_bf16_every_kernel():
     A, B = inputs.make(w)
     C_ref, Cabs = oracle.gemm(A, B)
     for kernel in ("auto", "tc_128x128", "tc_128x256", "tc_256x256", "tc_256x128", "simt", "simt_tpb3"):
-        tolerance_check(run_gpu(A, B, _out(w), kernel), C_ref, Cabs, with_output_rounding=False)
+        tolerance_check(run_gpu(A, B, _out(w), kernel), C_ref, Cabs)
 
 
-def _sums_check(C_gpu, A, B):
-    """Row and column sums of C against FP64 sums of the products; the bound
-    is the per-element bound summed (plus the output rounding of each
-    element for 16-bit outputs)."""
-    Ad, Bd = A.double(), B.double()
-    Cd = C_gpu.double()
-    rnd = HALF_ULP[C_gpu.dtype] if C_gpu.dtype != torch.float32 else 0.0
-    # rows: sum_j C[i, j] = A[i, :] . (B 1)
-    ref_r = (Ad @ Bd.sum(1)).numpy()
-    abs_r = (Ad.abs() @ Bd.abs().sum(1)).numpy()
-    got_r = Cd.sum(1).numpy()
-    bound_r = 1e-3 * abs_r + 1e-6 * C_gpu.shape[1] + rnd * Cd.abs().sum(1).numpy()
-    assert np.all(np.abs(got_r - ref_r) <= bound_r)
-    # columns: sum_i C[i, j] = (1^T A) . B[:, j]
-    ref_c = (Ad.sum(0) @ Bd).numpy()
-    abs_c = (Ad.abs().sum(0) @ Bd.abs()).numpy()
-    got_c = Cd.sum(0).numpy()
-    bound_c = 1e-3 * abs_c + 1e-6 * C_gpu.shape[0] + rnd * Cd.abs().sum(0).numpy()
-    assert np.all(np.abs(got_c - ref_c) <= bound_c)
+def _full_check(C_gpu, C_ref, Cabs):
+    """Every element of C within the stated bound; returns the worst
+    err / bound ratio."""
+    assert C_gpu.shape == C_ref.shape
+    got = C_gpu.double().numpy()
+    assert np.all(np.isfinite(got)), "non-finite output"
+    err = np.abs(got - C_ref)
+    bound = oracle.tolerance(Cabs)
+    bad = err > bound
+    if bad.any():
+        i, j = np.argwhere(bad)[0]
+        raise AssertionError(f"{int(bad.sum())} of {bad.size} elements out of bound, first "
+                             f"({i}, {j}): got {got[i, j]}, want {C_ref[i, j]}, bound {bound[i, j]}")
+    return float(np.max(err / bound))
 
 
 @pytest.mark.parametrize("name", ["square_4096_f16", "square_8192_bf16"])
-def test_large_workload_sampled(name):
+def test_large_workload_every_element(name):
+    """The whole output of the benchmarked call (gemm_ex_ws: whole waves of
+    256 x 256 pair tiles plus the last, partial wave split along K) and of
+    plain gemm_ex, element by element against the full oracle product; the
+    benchmarked call is also identical from one run to the next."""
     w = inputs.WORKLOADS[name]
     A, B = inputs.make(w)
-    C = run_gpu(A, B, _out(w), "auto")
-    assert C.shape == (w.M, w.N)
-    assert torch.isfinite(C.float()).all()
-    rows, cols = sample_indices(w.M, w.N, 3000, seed=w.seed, tile_m=256, tile_n=256)
-    ref, ref_abs = oracle.gemm_entries(A, B, rows, cols)
-    got = C[torch.from_numpy(rows), torch.from_numpy(cols)].double().numpy()
-    # the stated bound, with no allowance for the output rounding
-    assert np.all(np.abs(got - ref) <= oracle.tolerance(ref_abs))
-    _sums_check(C, A, B)
-    # run-to-run determinism at full size
-    C2 = run_gpu(A, B, _out(w), "auto")
-    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+    odt = _out(w)
+    dA, dB = A.cuda(), B.cuda()
+    C_ws = tg.matmul_ws(dA, dB, out_dtype=odt)
+    C_ws2 = tg.matmul_ws(dA, dB, out_dtype=odt)
+    C_plain = tg.matmul(dA, dB, out_dtype=odt)
+    assert tg.gemm_device_status(torch.cuda.current_stream().cuda_stream) == tg.binding.OK
+    assert torch.equal(C_ws.view(torch.int16), C_ws2.view(torch.int16))
+    C_ws, C_plain = C_ws.cpu(), C_plain.cpu()
+    del dA, dB, C_ws2
+    C_ref, Cabs = oracle.gemm(A, B, nthreads=os.cpu_count())
+    worst_ws = _full_check(C_ws, C_ref, Cabs)
+    worst_plain = _full_check(C_plain, C_ref, Cabs)
+    print(f"{name}: worst err/bound {worst_ws:.3f} (gemm_ex_ws), {worst_plain:.3f} (gemm_ex)")
 
 
 def test_tall_product_many_tiles():
     """M = 131072 rows (512 pair tiles, 1024 single-CTA tiles) with a short K:
-    sampled entries within the bound, row and column sums, on the automatic
-    choice and on gemm_ex_ws."""
+    every element within the bound, on the automatic choice and on
+    gemm_ex_ws."""
     A, B = inputs.draw(131072, 256, 136, "bf16", "normal", seed=30)
+    C_ref, Cabs = oracle.gemm(A, B, nthreads=os.cpu_count())
     for C in (run_gpu(A, B, torch.bfloat16, "auto"),
               tg.matmul_ws(A.cuda(), B.cuda(), out_dtype=torch.bfloat16).cpu()):
-        rows, cols = sample_indices(131072, 256, 4000, seed=31, tile_m=256, tile_n=256)
-        ref, ref_abs = oracle.gemm_entries(A, B, rows, cols)
-        got = C[torch.from_numpy(rows), torch.from_numpy(cols)].double().numpy()
-        half_ulp = HALF_ULP[torch.bfloat16] * np.abs(ref)
-        assert np.all(np.abs(got - ref) <= oracle.tolerance(ref_abs) + half_ulp)
-        _sums_check(C, A, B)
+        _full_check(C, C_ref, Cabs)
 
 
 @pytest.mark.parametrize("M, N, K, out_dtype", [

@@ -51,25 +51,36 @@ def _int_loop(A, B):
     return [[sum(A[i][k] * B[k][j] for k in range(K)) for j in range(N)] for i in range(M)]
 
 
+def _check_against_int_loop(M, N, K, dtype, seed):
+    A, B = inputs.draw(M, N, K, dtype, "int", seed=seed)
+    C, Cabs = oracle.gemm(A, B, nthreads=1)
+    Ai = A.to(torch.int64).tolist()
+    Bi = B.to(torch.int64).tolist()
+    want = np.array(_int_loop(Ai, Bi), dtype=np.float64)
+    want_abs = np.array(_int_loop([[abs(v) for v in r] for r in Ai],
+                                  [[abs(v) for v in r] for r in Bi]), dtype=np.float64)
+    np.testing.assert_array_equal(C, want)
+    np.testing.assert_array_equal(Cabs, want_abs)
+
+
+def test_brute_force_every_tiny_shape():
+    """Every (M, N, K) in {1..17}^3 (4913 shapes), integer inputs in [-4, 4]
+    (exact in every storage type), against integer arithmetic; the storage
+    type cycles F32, F16, BF16 from one shape to the next."""
+    dtypes = ("f32", "f16", "bf16")
+    for idx, (M, N, K) in enumerate(itertools.product(range(1, 18), repeat=3)):
+        _check_against_int_loop(M, N, K, dtypes[idx % 3], seed=idx)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-def test_brute_force_small_shapes(dtype):
-    """All M, N, K in {1..17} (sampled) plus 63/65/129 edges, integer inputs in
-    [-4, 4] (exact in every storage type), against integer arithmetic."""
-    rng = np.random.default_rng(7)
-    dims = list(range(1, 18)) + [63, 65, 129]
-    shapes = [(m, n, k) for m in dims for n in dims for k in dims]
-    picks = rng.choice(len(shapes), size=60, replace=False)
-    for idx in picks:
-        M, N, K = shapes[idx]
-        A, B = inputs.draw(M, N, K, dtype, "int", seed=int(idx))
-        C, Cabs = oracle.gemm(A, B, nthreads=3)
-        Ai = A.to(torch.int64).tolist()
-        Bi = B.to(torch.int64).tolist()
-        want = np.array(_int_loop(Ai, Bi), dtype=np.float64)
-        want_abs = np.array(_int_loop([[abs(v) for v in r] for r in Ai],
-                                      [[abs(v) for v in r] for r in Bi]), dtype=np.float64)
-        np.testing.assert_array_equal(C, want)
-        np.testing.assert_array_equal(Cabs, want_abs)
+def test_brute_force_tile_edge_shapes(dtype):
+    """Every (M, N, K) with each dimension in {63, 65, 129} or {1, 17}: one
+    below and one above a 64-wide tile, and one past two of them."""
+    dims = (1, 17, 63, 65, 129)
+    for idx, (M, N, K) in enumerate(itertools.product(dims, repeat=3)):
+        if max(M, N, K) < 63:
+            continue
+        _check_against_int_loop(M, N, K, dtype, seed=1000 + idx)
 
 
 def test_not_transposed_and_not_symmetric():

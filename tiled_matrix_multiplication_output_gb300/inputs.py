@@ -42,7 +42,7 @@ class Workload:
     K: int
     in_dtype: str
     out_dtype: str
-    dist: str          # "worked", "uniform", "normal_scaled", "normal", "int"
+    dist: str          # "worked", "uniform", "positive", "normal_scaled", "normal", "int"
     seed: int
 
     @property
@@ -73,8 +73,9 @@ def draw(M: int, N: int, K: int, in_dtype: str, dist: str, seed: int,
     """Draw A (M x K) then B (K x N) in FP32 with one seeded generator and
     round both to ``in_dtype``.
 
-    dist: "uniform" U[-1, 1]; "normal" N(0, 1); "normal_scaled" N(0, 1)/sqrt(K);
-    "int" integers uniform on [lo, hi] (exact in every input type).
+    dist: "uniform" U[-1, 1]; "positive" U[0, 1] (every product the same
+    sign); "normal" N(0, 1); "normal_scaled" N(0, 1)/sqrt(K); "int" integers
+    uniform on [lo, hi] (exact in every input type).
     """
     g = torch.Generator().manual_seed(seed)
     shapes = ((M, K), (K, N))
@@ -82,6 +83,8 @@ def draw(M: int, N: int, K: int, in_dtype: str, dist: str, seed: int,
     for shape in shapes:
         if dist == "uniform":
             x = torch.rand(shape, generator=g, dtype=torch.float32) * 2 - 1
+        elif dist == "positive":
+            x = torch.rand(shape, generator=g, dtype=torch.float32)
         elif dist == "normal":
             x = torch.randn(shape, generator=g, dtype=torch.float32)
         elif dist == "normal_scaled":
