@@ -10,10 +10,15 @@ Prints ONE JSON line (rank 0).  Keys beyond the common ones:
   roofline      dominant kernel vs the measured dense BF16 tensor peak, or vs the
                 measured HBM copy bandwidth for workloads below the ridge point
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
-  e2e           the same metric through gemm_ex_host with pinned host
+  sustained     the same step repeated for about 2.5 s after the timed region,
+                with its own clock record (the power-capped rate)
+  e2e           the same metric through gemm_ex_host_ws with pinned host
                 buffers (host-to-device copies of A, B and the device-to-host
-                copy of C inside the timed region)
+                copy of C inside the timed region), with the host link's
+                measured GB/s and the time the copies alone allow
   clocks        SM clocks and throttle reasons sampled during the timed loop
+  small_workloads  the three small named workloads: GPU time, cuBLAS time,
+                and the CPU oracle on all host cores and on one thread
 
 `--impl reference` times the CPU oracle instead (the only comparison arm:
 the pages publish no implementation).  With --gpus N > 1 (under torchrun)
@@ -295,6 +300,15 @@ def run_reference(args, rank, world):
 
 L2_BYTES = 129e6   # GB300 L2 capacity
 ALU_SMS = 152      # GB300 SMs, for the FP32 FMA peak
+# Dense FP16/BF16 tensor rate of one SM: a cta_group::1 tcgen05.mma of
+# M=128, N=256, K=16 (524,288 multiply-adds) takes 128 cycles, i.e. 4096
+# multiply-adds = 8192 FLOP per cycle per SM.
+TENSOR_FLOP_PER_SM_CYCLE = 8192
+
+
+def theoretical_tensor_tflops(sms: int, mhz: float) -> float:
+    """Dense FP16/BF16 tensor peak: SMs x 8192 FLOP per cycle x clock."""
+    return sms * TENSOR_FLOP_PER_SM_CYCLE * mhz * 1e6 / 1e12
 
 
 def footprint_bytes(w):
@@ -309,14 +323,17 @@ def needs_flush(w) -> bool:
     return footprint_bytes(w) <= L2_BYTES
 
 
-def roofline_of(w, flops, avg_launch_ms, peaks, peak_kind, traffic):
+def roofline_of(w, flops, avg_launch_ms, peaks, peak_kind, traffic, sms=ALU_SMS, run_mhz=None):
     """The roofline object for one workload.  The bound follows from the
     arithmetic intensity (FLOPs per compulsory byte of A, B and C) against
     the ridge point of the compute peak over the HBM peak: below it the
     workload is HBM-bound (achieved = compulsory bytes / time, against the
     measured copy bandwidth), above it compute-bound -- the tensor cores for
     16-bit inputs (measured cuBLAS BF16 peak), the FP32 FMA pipes for FP32
-    inputs (peak derived: SMs x 128 lanes x 2 FLOP x the maximum SM clock)."""
+    inputs (peak derived: SMs x 128 lanes x 2 FLOP x the maximum SM clock).
+    A tensor-bound line also carries the theoretical dense peak (SMs x 8192
+    FLOP per cycle x the maximum SM clock, and x the clock sampled during
+    the run when run_mhz is given) and the fractions of both."""
     seconds = avg_launch_ms * 1e-3
     nbytes = footprint_bytes(w)
     hbm = float(peaks["hbm_gbs"])
@@ -340,6 +357,18 @@ def roofline_of(w, flops, avg_launch_ms, peaks, peak_kind, traffic):
             "peak_source": source}
     if kind == "tensor":
         line["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+        max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        theo = theoretical_tensor_tflops(sms, max_mhz)
+        line["theoretical_peak"] = theo
+        line["frac_of_theoretical"] = achieved / theo
+        line["theoretical_source"] = (f"{sms} SMs x {TENSOR_FLOP_PER_SM_CYCLE} dense FP16/BF16 "
+                                      f"FLOP per cycle (one 128x256x16 tcgen05.mma per 128 "
+                                      f"cycles) x {max_mhz:.0f} MHz maximum SM clock")
+        if run_mhz:
+            at_run = theoretical_tensor_tflops(sms, float(run_mhz))
+            line["theoretical_peak_at_run_clock"] = at_run
+            line["frac_of_theoretical_at_run_clock"] = achieved / at_run
+            line["run_clock_mhz"] = float(run_mhz)
     return line
 
 
@@ -377,6 +406,127 @@ def timed_loop(fn, steps, stream, flush_buf):
     torch.cuda.synchronize(stream.device)
     per = [es[i].elapsed_time(ee[i]) for i in range(steps)]
     return sum(per), per
+
+
+def sustained_leg(fn, ms_per_step, stream, flush_buf, gpu_index, seconds=2.5, max_steps=20000):
+    """Back-to-back steps for about `seconds` of step time after the timed
+    region, with their own clock record: the rate once the power cap has
+    settled, where the timed region may be a short burst."""
+    steps = int(max(10, min(max_steps, math.ceil(seconds * 1e3 / max(ms_per_step, 1e-4)))))
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.25)
+    total_ms, _ = timed_loop(fn, steps, stream, flush_buf)
+    clocks = sampler.stop()
+    return steps, total_ms, clocks
+
+
+def link_rates(host_in, dev_in, dev_out, host_out, stream, reps=5):
+    """Host link GB/s from pinned buffers: host-to-device copies of the
+    inputs alone, the device-to-host copy of the output alone, and both at
+    once on two streams (median of `reps`, CUDA events)."""
+    import torch
+    side = torch.cuda.Stream(device=stream.device)
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host_in)
+    d2h_bytes = host_out.numel() * host_out.element_size()
+
+    def timed(kind):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(stream.device)
+        e0.record(stream)
+        side.wait_event(e0)
+        if kind in ("h2d", "both"):
+            with torch.cuda.stream(stream):
+                for d, h in zip(dev_in, host_in):
+                    d.copy_(h, non_blocking=True)
+        if kind in ("d2h", "both"):
+            with torch.cuda.stream(side if kind == "both" else stream):
+                host_out.copy_(dev_out, non_blocking=True)
+        if kind == "both":
+            stream.wait_stream(side)
+        e1.record(stream)
+        torch.cuda.synchronize(stream.device)
+        return e0.elapsed_time(e1)
+
+    out = {}
+    for kind, nbytes in (("h2d", h2d_bytes), ("d2h", d2h_bytes), ("both", h2d_bytes + d2h_bytes)):
+        timed(kind)
+        ms = statistics.median(timed(kind) for _ in range(reps))
+        out[f"{kind}_gbs"] = nbytes / (ms * 1e-3) / 1e9
+        out[f"{kind}_ms"] = ms
+    return out
+
+
+SMALL_WORKLOADS = ("worked_9x9", "square_128_f16", "edge_96x200x1000_bf16")
+
+
+def oracle_seconds(A, B, threads, min_seconds=0.2, min_reps=3):
+    """Median wall time of one full oracle product on `threads` threads."""
+    import oracle
+    times = []
+    t_end = time.perf_counter() + min_seconds
+    while len(times) < min_reps or time.perf_counter() < t_end:
+        t0 = time.perf_counter()
+        oracle.gemm(A, B, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+        if len(times) >= 1000:
+            break
+    return statistics.median(times)
+
+
+def small_workload_lines(dev, flush_buf_bytes):
+    """For each small named workload: the GPU time of the benchmarked call
+    (gemm_ex_ws, automatic choice; median of 200 steps with L2 overwritten
+    between them), cuBLAS on the same 16-bit inputs, and the full CPU
+    oracle product on all host cores and on one thread."""
+    import torch
+    import oracle
+    import tiled_matrix_multiplication_output_gb300 as tg
+    from tiled_matrix_multiplication_output_gb300 import binding, inputs
+    oracle.build()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(int(flush_buf_bytes), dtype=torch.uint8, device=dev)
+    threads = os.cpu_count() or 1
+    lines = []
+    for name in SMALL_WORKLOADS:
+        w = inputs.WORKLOADS[name]
+        A_cpu, B_cpu = inputs.make(w)
+        A, B = A_cpu.to(dev), B_cpu.to(dev)
+        C = torch.empty((w.M, w.N), dtype=binding.torch_dtype(w.out_dtype), device=dev)
+        ws_bytes = max(16, tg.gemm_workspace_size(w.M, w.N, w.K))
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        in_code, out_code = binding.dtype_code(w.in_dtype), binding.dtype_code(w.out_dtype)
+
+        def step():
+            rc = tg.gemm_ex_ws(A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, in_code,
+                               tg.F32, out_code, ws.data_ptr(), ws_bytes, stream.cuda_stream)
+            if rc != 0:
+                raise tg.GemmError(rc, "gemm_ex_ws")
+
+        for _ in range(5):
+            step()
+        _, per = timed_loop(step, 200, stream, flush)
+        gpu_us = statistics.median(per) * 1e3
+        line = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "in_dtype": w.in_dtype,
+                "out_dtype": w.out_dtype, "gpu_us": gpu_us,
+                "gpu_tflops": w.flops / (gpu_us * 1e-6) / 1e12,
+                "gpu_gbs_compulsory": footprint_bytes(w) / (gpu_us * 1e-6) / 1e9}
+        if w.in_dtype != "f32":
+            for _ in range(5):
+                torch.matmul(A, B)
+            _, per = timed_loop(lambda: torch.matmul(A, B), 200, stream, flush)
+            line["cublas_us"] = statistics.median(per) * 1e3
+        cpu = {}
+        for label, nthr in (("all_cores", threads), ("one_thread", 1)):
+            sec = oracle_seconds(A_cpu, B_cpu, nthr)
+            cpu[label] = {"value": w.flops / sec / 1e12, "unit": UNIT, "us": sec * 1e6,
+                          "cores": min(nthr, w.M)}
+        line["cpu_baseline"] = {"kind": "oracle", "sample": "the whole product", **cpu}
+        lines.append(line)
+        del A, B, C, ws
+    del flush
+    return lines
 
 
 def run_ours(args, rank, world, local):
@@ -460,6 +610,13 @@ def run_ours(args, rank, world, local):
                               "gpu_launches": launches, "kernel_only": True}), flush=True)
         return
 
+    # ---- the same step held for seconds: the power-capped rate
+    sus_steps, sus_ms, sus_clocks = sustained_leg(step, ms_per_step, stream, flush_buf, local)
+    sus_ms = max_over_ranks(sus_ms, world)
+    sustained = {"value": job_rate(flops, sus_steps, world, sus_ms), "unit": UNIT,
+                 "steps": sus_steps, "ms_per_step": sus_ms / sus_steps,
+                 "seconds": sus_ms * 1e-3, "clocks": sus_clocks}
+
     # ---- end to end through the host-buffer entry point
     in_b = 4 if w.in_dtype == "f32" else 2
     out_b = 4 if w.out_dtype == "f32" else 2
@@ -469,11 +626,11 @@ def run_ours(args, rank, world, local):
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
 
     def host_step():
-        rc = tg.gemm_ex_host(Ah.data_ptr(), Bh.data_ptr(), Ch.data_ptr(), w.M, w.N, w.K,
-                             in_code, tg.F32, out_code, A.data_ptr(), B.data_ptr(),
-                             C.data_ptr(), sh)
+        rc = tg.gemm_ex_host_ws(Ah.data_ptr(), Bh.data_ptr(), Ch.data_ptr(), w.M, w.N, w.K,
+                                in_code, tg.F32, out_code, A.data_ptr(), B.data_ptr(),
+                                C.data_ptr(), ws.data_ptr(), ws_bytes if use_ws else 0, sh)
         if rc != 0:
-            raise tg.GemmError(rc, "gemm_ex_host")
+            raise tg.GemmError(rc, "gemm_ex_host_ws")
 
     for _ in range(3):
         host_step()
@@ -488,13 +645,26 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+    h2d_bytes = (w.M * w.K + w.K * w.N) * in_b
+    d2h_bytes = w.M * w.N * out_b
+    link = link_rates((Ah, Bh), (A, B), C, Ch, stream)
+    panel_rows = tg.gemm_host_panel_rows(w.M)
+    panels = max(1, -(-w.M // max(1, panel_rows)))
+    # what the copies alone allow: every byte over the link with both
+    # directions busy, plus the one panel's product that cannot overlap a copy
+    model_ms = (h2d_bytes + d2h_bytes) / (link["both_gbs"] * 1e9) * 1e3 + ms_per_step / panels
+    link.update({"panels": panels, "panel_rows": panel_rows, "model_ms": model_ms, "e2e_over_model": e2e_ms / model_ms,
+                 "achieved_gbs": (h2d_bytes + d2h_bytes) / (e2e_ms * 1e-3) / 1e9})
 
     # ---- cuBLAS on the same inputs, as context only
     for _ in range(5):
         torch.matmul(A, B)
-    n_cublas = args.steps   # same length as our timed loop, so both run at sustained clocks
+    n_cublas = args.steps   # same length as our timed loop
     cublas_ms, _ = timed_loop(lambda: torch.matmul(A, B), n_cublas, stream, flush_buf)
     cublas_tflops = flops * n_cublas / (cublas_ms * 1e-3) / 1e12
+    cb_steps, cb_ms, cb_clocks = sustained_leg(lambda: torch.matmul(A, B), cublas_ms / n_cublas,
+                                               stream, flush_buf, local)
+    cublas_sustained = flops * cb_steps / (cb_ms * 1e-3) / 1e12
 
     if rank != 0:
         return
@@ -503,18 +673,30 @@ def run_ours(args, rank, world, local):
     base_kernel = kname.split("+")[0]
     traffic = committed_traffic(
         f"tc_gemm_{base_kernel[3:]}" if base_kernel.startswith("tc_") else base_kernel, w.name)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    roofline = roofline_of(w, flops, avg_launch_ms, peaks, peak_kind, traffic, sms=sms,
+                           run_mhz=(clocks or {}).get("sm_mhz"))
+    if roofline["bound"] == "tensor":
+        sustained["frac_of_sustained_peak"] = sustained["value"] / float(
+            peaks["bf16_tflops_sustained"])
+        if sus_clocks and sus_clocks.get("sm_mhz"):
+            sustained["frac_of_theoretical_at_run_clock"] = sustained["value"] / (
+                theoretical_tensor_tflops(sms, sus_clocks["sm_mhz"]) * world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.in_dtype, "data": "synthetic",
         "config": config_of(w, kname),
-        "roofline": roofline_of(w, flops, avg_launch_ms, peaks, peak_kind, traffic),
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": (w.M * w.K + w.K * w.N) * in_b,
-                "d2h_bytes_per_step": w.M * w.N * out_b, "steps": e2e_steps,
-                "entry_point": "gemm_ex_host (pinned host buffers)"},
+        "roofline": roofline,
+        "sustained": sustained,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps, "ms_per_step": e2e_ms,
+                "entry_point": "gemm_ex_host_ws (pinned host buffers, the same workspace)",
+                "link": link},
         "gpu_launches": launches,
         "clocks": clocks,
         "context": {"cublas_torch_matmul_tflops": cublas_tflops,
+                    "cublas_sustained_tflops": cublas_sustained, "cublas_sustained_clocks": cb_clocks,
                     "per_launch_ms_min": min(per_launch), "per_launch_ms_median":
                     statistics.median(per_launch)},
     }
@@ -523,6 +705,8 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"] = {
             "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {rows} of {w.M} rows of C ({rows}x{w.N}x{w.K}), {secs:.1f} s"}
+        if w.name not in SMALL_WORKLOADS:
+            line["small_workloads"] = small_workload_lines(dev, 2 * L2_BYTES)
     print(json.dumps(line), flush=True)
 
 
