@@ -498,3 +498,41 @@ def test_fp32_accumulator_overflow(kernel):
         want = oracle.round_to(C_ref, out).double().numpy()
         assert np.isinf(want[:, : N // 2]).all() and np.isfinite(want[:, N // 2:]).all()
         np.testing.assert_array_equal(run_gpu(A, B, out, kernel).double().numpy(), want)
+
+
+@pytest.mark.parametrize("op_a,op_b", [("n", "n"), ("t", "n"), ("n", "t"), ("t", "t")])
+def test_simt_f32_wide_load_kernel_exact(op_a, op_b):
+    """FP32 operands whose stored rows are multiples of 4 elements take the
+    large-tile SIMT kernel with 16-byte loads: ragged M and N (2060 = 16 *
+    128 + 12 rows, 1292 = 10 * 128 + 12 columns) with 1, 2, 3 and 7 K tiles
+    of 16, the last one partial; and 2600 x 2600 (441 tiles, more than the
+    resident blocks) so blocks restart on a second tile.  Integer inputs,
+    exact against the oracle's general form, every layout."""
+    for M, N, K, seed in ((2060, 1292, 4, 90), (2060, 1292, 12, 91), (2060, 1292, 20, 92),
+                          (2060, 1292, 36, 93), (2060, 1292, 100, 94), (2600, 2600, 36, 95)):
+        A0, B0 = inputs.draw(M, N, K, "f32", "int", seed=seed)
+        A = A0.t().contiguous() if op_a == "t" else A0
+        B = B0.t().contiguous() if op_b == "t" else B0
+        C = tg.addmm(A.cuda(), B.cuda(), op_a=op_a, op_b=op_b, out_dtype=torch.float32,
+                     kernel="simt").cpu()
+        ref, _ = oracle.gemm_general(A, B, op_a, op_b)
+        np.testing.assert_array_equal(C.double().numpy(), ref,
+                                      err_msg=f"{M}x{N}x{K} layout {op_a}{op_b}")
+
+
+def test_simt_f32_wide_load_kernel_outputs_and_addmm():
+    """The same kernel with 16-bit outputs (element stores), alpha and beta
+    (C read back), and the 16-byte FP32 stores on full-width tiles beside
+    element stores on the ragged last column of tiles."""
+    M, N, K = 2048, 1548, 40                       # 1548 = 12 * 128 + 12
+    A, B = inputs.draw(M, N, K, "f32", "int", seed=96)
+    for out in (torch.float16, torch.bfloat16, torch.float32):
+        expect_exact(run_gpu(A, B, out, "simt"), A, B)
+    Cin = inputs.draw(M, 1, N, "f32", "int", seed=97)[0]
+    C = tg.addmm(A.cuda(), B.cuda(), Cin.clone().cuda(), alpha=2.0, beta=-1.0,
+                 out_dtype=torch.float32, kernel="simt").cpu()
+    ref, _ = oracle.gemm_general(A, B, alpha=2.0, beta=-1.0, C_in=Cin)
+    np.testing.assert_array_equal(C.double().numpy(), ref)
+    # random FP32 inputs: within the stated bound
+    A, B = inputs.draw(M, N, 1000, "f32", "normal", seed=98)
+    expect_close(run_gpu(A, B, torch.float32, "simt"), A, B)

@@ -99,14 +99,21 @@ def test_large_workload_every_element(name):
     print(f"{name}: worst err/bound {worst_ws:.3f} (gemm_ex_ws), {worst_plain:.3f} (gemm_ex)")
 
 
-def test_tall_product_many_tiles():
-    """M = 131072 rows (512 pair tiles, 1024 single-CTA tiles) with a short K:
-    every element within the bound, on the automatic choice and on
-    gemm_ex_ws."""
-    A, B = inputs.draw(131072, 256, 136, "bf16", "normal", seed=30)
+@pytest.mark.parametrize("K, out_dtype", [(136, torch.float32), (1032, torch.bfloat16)])
+def test_tall_product_many_tiles(K, out_dtype):
+    """M = 131072 rows (512 pair tiles, 1024 single-CTA tiles): every element
+    within the stated bound, on the automatic choice and on gemm_ex_ws.
+
+    The short K runs with an FP32 output.  A BF16 output adds its own final
+    rounding, up to 2^-9 |C|, which exceeds 1e-3 sum|ab| wherever |C| >
+    0.51 sum|ab|; among 33.5 M random-sign entries with K = 136 some do
+    (|C| reaches 0.4-0.5 sum|ab| in the tails), whatever the kernel.  At
+    K = 1032 the largest ratio is about 0.27, so the BF16 output meets the
+    bound as stated."""
+    A, B = inputs.draw(131072, 256, K, "bf16", "normal", seed=30)
     C_ref, Cabs = oracle.gemm(A, B, nthreads=os.cpu_count())
-    for C in (run_gpu(A, B, torch.bfloat16, "auto"),
-              tg.matmul_ws(A.cuda(), B.cuda(), out_dtype=torch.bfloat16).cpu()):
+    for C in (run_gpu(A, B, out_dtype, "auto"),
+              tg.matmul_ws(A.cuda(), B.cuda(), out_dtype=out_dtype).cpu()):
         _full_check(C, C_ref, Cabs)
 
 

@@ -35,6 +35,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 
 #include "launch.h"
 
@@ -374,6 +375,258 @@ __global__ void __launch_bounds__(256, 2)
     }
 }
 
+// FP32 operands whose rows start on 16-byte boundaries (base addresses
+// 16-byte aligned; the contiguous dimension of each stored operand a
+// multiple of 4): the large-tile kernel with 16-byte global loads.  A
+// 128 x 128 block tile, K tiles of 16, an 8 x 8 micro-tile per thread laid
+// out as in simt_gemm_big_kernel.  Each thread moves two 16-byte words of
+// each operand per K tile; words that run along k in memory (A as stored, B
+// transposed) are scattered into the K-major shared tile as four 4-byte
+// stores, words that run along m or n (A transposed, B as stored) land as
+// one 16-byte store.  With K % 4 == 0 (or M, N % 4 == 0 for the transposed
+// forms) a word is either wholly inside the matrix or wholly outside it, so
+// one guard per word keeps ragged edges exact.
+//
+// With B as stored, the multiply-adds run in pairs: fma.rn.f32x2 performs
+// two IEEE single-precision fused multiply-adds (columns 2p and 2p + 1 of a
+// micro-tile row) in one instruction, so a K step issues 32 instructions
+// for its 64 multiply-adds and leaves issue slots for the fragment loads.
+// Each result is the same fused multiply-add as fmaf, in the same order.
+// Measured on GB300 (FP32, 4096^3, TFLOP/s, paired / single): A and B as
+// stored 56.7 / 50.3, A transposed 55.8 / 51.0; with B transposed the
+// paired form needs more registers than two blocks per SM leave and lost
+// (52.8 / 55.1, 51.5 / 52.9), so those layouts issue single FMAs.
+template <typename OutT, bool OP_A, bool OP_B>
+__global__ void __launch_bounds__(256, 2)
+    simt_gemm_f32v_kernel(const float* __restrict__ A, const float* __restrict__ B, OutT* C,
+                          int M, int N, int K, float alpha, float beta)
+{
+    constexpr int BM = 128, BN = 128, BK = 16, NT = 256, LD = BM + 4;
+    constexpr bool PAIRED = !OP_B;
+    // words per thread per operand and K tile: BM * BK / 4 / NT
+    constexpr int WA = BM * BK / 4 / NT, WB = BK * BN / 4 / NT;
+    __shared__ __align__(16) float As[2][BK][LD];
+    __shared__ __align__(16) float Bs[2][BK][LD];
+
+    const int tid = threadIdx.x;
+    const int tx = tid & 15;
+    const int ty = tid >> 4;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int tiles_m = (M + BM - 1) / BM;
+    const long long num_tiles = static_cast<long long>(tiles_m) * tiles_n;
+
+    // Word w of a thread is word tid + NT * w of the tile, counted along the
+    // contiguous dimension.  A as stored (M x K): a row holds BK / 4 words,
+    // so word w sits at row tid / 4 + 64 w, k (tid % 4) * 4.  A transposed
+    // (K x M): a k-row holds 32 words, so word w sits at k-row tid / 32 +
+    // 8 w, m (tid % 32) * 4.  B likewise (B as stored is like A transposed).
+    constexpr int KW = BK / 4;                       // words per row along k
+    const int a_r = OP_A ? tid / 32 : tid / KW;      // row (or k-row) of word 0
+    const int a_c = OP_A ? (tid % 32) * 4 : (tid % KW) * 4;
+    constexpr int A_DR = OP_A ? NT / 32 : NT / KW;   // rows from one word to the next
+    const int b_r = OP_B ? tid / KW : tid / 32;
+    const int b_c = OP_B ? (tid % KW) * 4 : (tid % 32) * 4;
+    constexpr int B_DR = OP_B ? NT / KW : NT / 32;
+
+    float4 ra[WA], rb[WB];
+    const float* a_ptr = A;
+    const float* b_ptr = B;
+    unsigned a_ok = 0, b_ok = 0;  // bit w: word w's m (or n) range lies inside C
+    const long long a_wstride = OP_A ? static_cast<long long>(A_DR) * M
+                                     : static_cast<long long>(A_DR) * K;
+    const long long b_wstride = OP_B ? static_cast<long long>(B_DR) * K
+                                     : static_cast<long long>(B_DR) * N;
+    const long long a_kstep = OP_A ? static_cast<long long>(BK) * M : BK;
+    const long long b_kstep = OP_B ? BK : static_cast<long long>(BK) * N;
+
+    auto set_tile = [&](int m0, int n0) {
+        a_ok = 0;
+        b_ok = 0;
+        if (OP_A) {
+            a_ptr = A + static_cast<long long>(a_r) * M + m0 + a_c;
+            if (m0 + a_c < M)
+                a_ok = (1u << WA) - 1;
+        } else {
+            a_ptr = A + static_cast<long long>(m0 + a_r) * K + a_c;
+#pragma unroll
+            for (int w = 0; w < WA; ++w)
+                a_ok |= (m0 + a_r + w * A_DR < M ? 1u : 0u) << w;
+        }
+        if (OP_B) {
+            b_ptr = B + static_cast<long long>(n0 + b_r) * K + b_c;
+#pragma unroll
+            for (int w = 0; w < WB; ++w)
+                b_ok |= (n0 + b_r + w * B_DR < N ? 1u : 0u) << w;
+        } else {
+            b_ptr = B + static_cast<long long>(b_r) * N + n0 + b_c;
+            if (n0 + b_c < N)
+                b_ok = (1u << WB) - 1;
+        }
+    };
+    // Loads K tile k0 (a_ptr, b_ptr already advanced to it).
+    auto load_tile = [&](int k0) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < WA; ++w) {
+            const int kk = OP_A ? k0 + a_r + w * A_DR : k0 + a_c;
+            ra[w] = ((a_ok >> w) & 1u) && kk < K
+                        ? __ldg(reinterpret_cast<const float4*>(a_ptr + w * a_wstride))
+                        : z;
+        }
+#pragma unroll
+        for (int w = 0; w < WB; ++w) {
+            const int kk = OP_B ? k0 + b_c : k0 + b_r + w * B_DR;
+            rb[w] = ((b_ok >> w) & 1u) && kk < K
+                        ? __ldg(reinterpret_cast<const float4*>(b_ptr + w * b_wstride))
+                        : z;
+        }
+    };
+    auto store_tile = [&](int buf) {
+#pragma unroll
+        for (int w = 0; w < WA; ++w) {
+            if (OP_A) {
+                *reinterpret_cast<float4*>(&As[buf][a_r + w * A_DR][a_c]) = ra[w];
+            } else {
+                const int r = a_r + w * A_DR;
+                As[buf][a_c + 0][r] = ra[w].x;
+                As[buf][a_c + 1][r] = ra[w].y;
+                As[buf][a_c + 2][r] = ra[w].z;
+                As[buf][a_c + 3][r] = ra[w].w;
+            }
+        }
+#pragma unroll
+        for (int w = 0; w < WB; ++w) {
+            if (OP_B) {
+                const int r = b_r + w * B_DR;
+                Bs[buf][b_c + 0][r] = rb[w].x;
+                Bs[buf][b_c + 1][r] = rb[w].y;
+                Bs[buf][b_c + 2][r] = rb[w].z;
+                Bs[buf][b_c + 3][r] = rb[w].w;
+            } else {
+                *reinterpret_cast<float4*>(&Bs[buf][b_r + w * B_DR][b_c]) = rb[w];
+            }
+        }
+    };
+
+    for (long long tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int m0 = static_cast<int>(tile / tiles_n) * BM;
+        const int n0 = static_cast<int>(tile % tiles_n) * BN;
+        // acc holds the micro-tile for single FMAs; acc2[i][p] columns 2p,
+        // 2p + 1 of row i for paired ones (only one of the two is used).
+        float acc[8][8];
+        float2 acc2[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                acc[i][j] = 0.0f;
+            if constexpr (PAIRED) {
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    acc2[i][p] = make_float2(0.0f, 0.0f);
+            }
+        }
+
+        // One K tile from shared buffer `buf`.  Odd micro-tile rows take the
+        // columns in reverse (the zig-zag order of simt_gemm_big_kernel).
+        auto multiply = [&](int buf) {
+#pragma unroll
+            for (int k = 0; k < BK; ++k) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * ty]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][64 + 4 * ty]);
+                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][4 * tx]);
+                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][64 + 4 * tx]);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                if constexpr (PAIRED) {
+                    const float2 b[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                         make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float2 ai = make_float2(a[i], a[i]);
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            const int p = (i & 1) ? 3 - pp : pp;
+                            acc2[i][p] = __ffma2_rn(ai, b[p], acc2[i][p]);
+                        }
+                    }
+                } else {
+                    const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int j = (i & 1) ? 7 - jj : jj;
+                            acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                        }
+                }
+            }
+        };
+
+        // K tile t is multiplied from buffer t & 1; tile t + 1 is loaded
+        // into registers before those multiplies and stored into the other
+        // buffer after them, one barrier per K tile (the previous output
+        // tile's last barrier follows all of its shared-memory reads).
+        set_tile(m0, n0);
+        const int nk = (K + BK - 1) / BK;
+        if (nk > 0) {
+            load_tile(0);
+            store_tile(0);
+            __syncthreads();
+        }
+        for (int t = 0; t < nk; ++t) {
+            const bool more = t + 1 < nk;
+            if (more) {
+                a_ptr += a_kstep;
+                b_ptr += b_kstep;
+                load_tile((t + 1) * BK);
+            }
+            multiply(t & 1);
+            if (more)
+                store_tile((t + 1) & 1);
+            __syncthreads();
+        }
+
+        if constexpr (PAIRED) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    acc[i][2 * p] = acc2[i][p].x;
+                    acc[i][2 * p + 1] = acc2[i][p].y;
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int gm = m0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
+            if (gm >= M)
+                continue;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int gn = n0 + (j < 4 ? 4 * tx + j : 64 + 4 * tx + j - 4);
+                if (gn < N) {
+                    OutT* dst = C + static_cast<long long>(gm) * N + gn;
+                    const float v = (beta != 0.0f) ? fmaf(beta, load_out(dst), alpha * acc[i][j])
+                                                   : alpha * acc[i][j];
+                    store_out(dst, v);
+                }
+            }
+        }
+    }
+}
+
+// Whether the 16-byte-load FP32 kernel can take these operands: FP32
+// inputs, 16-byte aligned bases, and rows of every stored operand a
+// multiple of 4 elements long.
+inline bool simt_f32v_ok(const SimtLaunch& l)
+{
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (l.in_dtype != DT_F32 || !al(l.A) || !al(l.B))
+        return false;
+    const int pitch_a = l.op_a ? l.M : l.K;
+    const int pitch_b = l.op_b ? l.K : l.N;
+    return pitch_a % 4 == 0 && pitch_b % 4 == 0;
+}
+
 template <int BM, int BN, int BK, int TM, int TN, typename InT, typename OutT>
 cudaError_t launch_simt(const SimtLaunch& l, cudaStream_t stream)
 {
@@ -383,6 +636,27 @@ cudaError_t launch_simt(const SimtLaunch& l, cudaStream_t stream)
     if (BM == 64 && big_tiles >= l.num_sms) {
         const long long cap = static_cast<long long>(std::max(l.num_sms, 1)) * 2;
         const int grid = static_cast<int>(std::max<long long>(1, std::min(big_tiles, cap)));
+        if constexpr (std::is_same<InT, float>::value) {
+            if (simt_f32v_ok(l)) {
+                note_launch();
+                const float* A = static_cast<const float*>(l.A);
+                const float* B = static_cast<const float*>(l.B);
+                OutT* C = static_cast<OutT*>(l.C);
+                if (!l.op_a && !l.op_b)
+                    simt_gemm_f32v_kernel<OutT, false, false>
+                        <<<grid, 256, 0, stream>>>(A, B, C, l.M, l.N, l.K, l.alpha, l.beta);
+                else if (l.op_a && !l.op_b)
+                    simt_gemm_f32v_kernel<OutT, true, false>
+                        <<<grid, 256, 0, stream>>>(A, B, C, l.M, l.N, l.K, l.alpha, l.beta);
+                else if (!l.op_a && l.op_b)
+                    simt_gemm_f32v_kernel<OutT, false, true>
+                        <<<grid, 256, 0, stream>>>(A, B, C, l.M, l.N, l.K, l.alpha, l.beta);
+                else
+                    simt_gemm_f32v_kernel<OutT, true, true>
+                        <<<grid, 256, 0, stream>>>(A, B, C, l.M, l.N, l.K, l.alpha, l.beta);
+                return cudaGetLastError();
+            }
+        }
         note_launch();
         const InT* A = static_cast<const InT*>(l.A);
         const InT* B = static_cast<const InT*>(l.B);
