@@ -78,7 +78,10 @@ typedef enum {
     GEMM_KERNEL_TC_128x128 = 3,/* tcgen05, one CTA per 128 x 128 output tile */
     GEMM_KERNEL_TC_128x256 = 4,/* tcgen05, one CTA per 128 x 256 output tile */
     GEMM_KERNEL_TC_256x256 = 5,/* tcgen05 cta_group::2, one CTA pair per 256 x 256 tile */
-    GEMM_KERNEL_TC_256x128 = 6 /* tcgen05 cta_group::2, one CTA pair per 256 x 128 tile */
+    GEMM_KERNEL_TC_256x128 = 6,/* tcgen05 cta_group::2, one CTA pair per 256 x 128 tile */
+    GEMM_KERNEL_TC_SMALL = 7   /* tcgen05, one CTA per 128 x 64 or 128 x 128 tile, not
+                                  persistent: the lowest fixed cost, for products whose
+                                  tiles fit in one wave */
 } gemm_kernel_t;
 
 /*

@@ -8,7 +8,7 @@ import torch
 import oracle
 import tiled_matrix_multiplication_output_gb300 as tg
 
-TC_KERNELS = ("tc_128x128", "tc_128x256", "tc_256x256", "tc_256x128")
+TC_KERNELS = ("tc_128x128", "tc_128x256", "tc_256x256", "tc_256x128", "tc_small")
 ALL_KERNELS = ("simt", "simt_tpb3") + TC_KERNELS
 
 # Half an ulp at 1.0 of each output type: the relative size of one

@@ -340,9 +340,10 @@ def test_host_buffer_entry_point_with_workspace(M, N, K, out_dtype):
 
 
 def test_automatic_choice_on_the_named_workloads():
-    """The cost model's picks on the named workloads: the single-CTA kernel
-    for one-tile problems (lowest fixed latency), the CTA-pair kernel for the
-    large squares, SIMT for FP32 and for shapes the tensor maps cannot take."""
+    """The automatic picks on the named workloads: the non-persistent
+    single-tile kernel when the tiles fit in one wave and K is short (lowest
+    fixed latency), the CTA-pair kernel for the large squares, SIMT for FP32
+    and for shapes the tensor maps cannot take."""
     def pick(M, N, K, in_dt, out_dt, dtype=torch.bfloat16):
         A = torch.zeros(M, K, dtype=dtype, device="cuda")
         B = torch.zeros(K, N, dtype=dtype, device="cuda")
@@ -350,8 +351,10 @@ def test_automatic_choice_on_the_named_workloads():
         return tg.KERNEL_NAMES[tg.gemm_select_kernel(A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                                      M, N, K, in_dt, tg.F32, out_dt)]
     assert pick(9, 9, 9, tg.F32, tg.F32, torch.float32) == "simt"
-    assert pick(128, 128, 128, tg.F16, tg.F32, torch.float16) == "tc_128x128"
-    assert pick(96, 200, 1000, tg.BF16, tg.F32) == "tc_128x128"
+    assert pick(128, 128, 128, tg.F16, tg.F32, torch.float16) == "tc_small"
+    assert pick(96, 200, 1000, tg.BF16, tg.F32) == "tc_small"
+    assert pick(512, 512, 512, tg.BF16, tg.BF16) == "tc_small"
+    assert pick(256, 256, 4096, tg.BF16, tg.F32) == "tc_128x128"   # split along K by gemm_ex_ws
     assert pick(4096, 4096, 4096, tg.F16, tg.F16, torch.float16) == "tc_256x256"
     assert pick(8192, 8192, 8192, tg.BF16, tg.BF16) == "tc_256x256"
 

@@ -77,17 +77,20 @@ def test_splitk_unaligned_falls_back_exactly():
 
 
 def test_gemm_ex_ws_splits_few_tile_products():
-    """gemm_ex_ws takes split-K for few output tiles and a long K (the
-    96 x 200 x 1000 workload's shape): two launches, bit for bit the result
-    of gemm_splitk with the reported count, on integer and on random inputs;
-    large products and short K are not split."""
-    M, N, K = 96, 200, 1000
+    """gemm_ex_ws takes split-K for few output tiles and a long K (32 K steps
+    or more; 96 x 200 x 4000 here): two launches, bit for bit the result of
+    gemm_splitk with the reported count, on integer and on random inputs;
+    large products and shorter K are not split (the 96 x 200 x 1000
+    workload runs on one CTA per tile in a single launch)."""
+    M, N, K = 96, 200, 4000
     count = tg.gemm_ws_split_count(M, N, K, tg.BF16, tg.F32, tg.F32)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert count == min(sms // 2, 8)      # 2 tiles, 16 K steps: up to one unit per SM, 8 ranges at most
+    assert count == min(sms // 2, 8)      # 2 tiles, 63 K steps: up to one unit per SM, 8 ranges at most
     assert tg.gemm_ws_split_count(8192, 8192, 8192, tg.BF16, tg.F32, tg.BF16) == 0
     assert tg.gemm_ws_split_count(128, 128, 128, tg.F16, tg.F32, tg.F32) == 0
-    assert tg.gemm_ws_split_count(96, 200, 1000, tg.F32, tg.F32, tg.F32) == 0   # SIMT path
+    assert tg.gemm_ws_split_count(96, 200, 1000, tg.BF16, tg.F32, tg.F32) == 0  # 16 K steps
+    assert tg.gemm_ws_split_count(96, 200, 2048, tg.BF16, tg.F32, tg.F32) >= 2  # 32 K steps
+    assert tg.gemm_ws_split_count(96, 200, 4000, tg.F32, tg.F32, tg.F32) == 0   # SIMT path
     assert tg.gemm_ws_split_count(-1, 200, 1000, tg.BF16, tg.F32, tg.F32) == -tg.binding.ERR_INVALID_VALUE
     A, B = inputs.draw(M, N, K, "bf16", "int", seed=31)
     dA, dB = A.cuda(), B.cuda()
@@ -119,7 +122,7 @@ def test_gemm_ex_ws_splits_few_tile_products():
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("shape", [(96, 200, 1000), (100, 136, 2056), (384, 256, 4096)])
+@pytest.mark.parametrize("shape", [(96, 200, 3000), (100, 136, 2056), (384, 256, 4096)])
 def test_gemm_ex_ws_few_tile_split_every_output_type(shape, out_dtype):
     """The few-tile split path of gemm_ex_ws on ragged shapes and every output
     type: exact on integer inputs, within the bound on random ones, and
@@ -146,3 +149,22 @@ def test_gemm_ex_ws_few_tile_split_every_output_type(shape, out_dtype):
         else:
             C_ref, Cabs = oracle.gemm(A, B)
             tolerance_check(outs[0].cpu(), C_ref, Cabs)
+
+
+def test_gemm_ex_ws_edge_workload_is_one_launch():
+    """The 96 x 200 x 1000 workload through gemm_ex_ws: 16 K steps are short
+    of the split threshold, so one launch of the single-tile kernel, exact
+    on integer inputs."""
+    M, N, K = 96, 200, 1000
+    A, B = inputs.draw(M, N, K, "bf16", "int", seed=34)
+    dA, dB = A.cuda(), B.cuda()
+    s = torch.cuda.current_stream().cuda_stream
+    ws_bytes = tg.gemm_workspace_size(M, N, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    C = torch.full((M, N), float("nan"), device="cuda")
+    n0 = tg.gemm_launch_count()
+    assert tg.gemm_ex_ws(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, tg.BF16, tg.F32,
+                         tg.F32, ws.data_ptr(), ws_bytes, s) == 0
+    assert tg.gemm_launch_count() - n0 == 1
+    assert tg.gemm_device_status(s) == 0
+    expect_exact(C.cpu(), A, B)

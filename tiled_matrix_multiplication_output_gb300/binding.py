@@ -34,6 +34,7 @@ KERNELS = {
     "tc_128x256": 4,
     "tc_256x256": 5,
     "tc_256x128": 6,
+    "tc_small": 7,
 }
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 

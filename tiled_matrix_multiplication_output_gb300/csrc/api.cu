@@ -116,6 +116,22 @@ bool tc_eligible(const Problem& q)
     return true;
 }
 
+// K steps from which a product with few output tiles is split along K
+// rather than run on one CTA per tile: below it, splitting K adds a second
+// launch and the partials' traffic for little gain (measured on GB300, L2
+// flushed, BF16: 512 x 512 x 1024 10.6 us on one CTA per tile against 12.3
+// split; 256 x 256 x 2048 14.8 against 12.3).
+constexpr int64_t kSplitMinKBlocks = 32;
+
+// Whether the non-persistent single-tile kernel takes a product: its tiles
+// fit in one wave of CTAs and K is short of kSplitMinKBlocks steps.
+bool small_kernel_fits(int64_t M, int64_t N, int64_t K, int num_sms)
+{
+    const int64_t bn = tc_small_tile_n(M, N, num_sms);
+    const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+    return tiles <= num_sms && (K + 63) / 64 < kSplitMinKBlocks;
+}
+
 // The automatic choice.  Tiny products go to the SIMT kernel (a tensor-core
 // launch has a fixed set-up cost); otherwise the tensor-core variant with the
 // smallest predicted time: the tile traffic of the loop nest, the waves of
@@ -129,6 +145,15 @@ int auto_kernel(const Problem& q, int num_sms)
     const double flops = 2.0 * double(M) * double(N) * double(K);
     if (flops < 2.0 * 64 * 64 * 64)
         return GEMM_KERNEL_SIMT;
+    // One wave of single-tile CTAs and a short K: the non-persistent kernel
+    // (tc_small.cu), the lowest fixed cost.  Measured on GB300 with L2
+    // flushed between calls (BF16, microseconds, against the 128 x 128
+    // persistent kernel): 64^3 6.8 / 7.4, 512^3 8.9 / 10.3, 256 x 256 x
+    // 1024 10.8 / 12.0, 96 x 200 x 1000 10.9 / 13.0, equal within 0.4 us up
+    // to 2048 x 1024 x 512.  From 32 K steps up, few tiles are split along K
+    // instead (gemm_ex_ws).
+    if (small_kernel_fits(M, N, K, num_sms))
+        return GEMM_KERNEL_TC_SMALL;
     const int in_b = dt_size(q.in_dtype), out_b = dt_size(q.out_dtype);
     int best = GEMM_KERNEL_TC_256x256;
     double best_t = predict_seconds(M, N, K, TC_256x256, num_sms, in_b, out_b);
@@ -157,7 +182,7 @@ int run(const Problem& q, int kernel, cudaStream_t stream)
     int rc = validate_problem(q);
     if (rc != GEMM_OK)
         return rc;
-    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_TC_256x128)
+    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_TC_SMALL)
         return GEMM_ERR_INVALID_VALUE;
     if (q.M == 0 || q.N == 0)
         return GEMM_OK;
@@ -187,7 +212,8 @@ int run(const Problem& q, int kernel, cudaStream_t stream)
         l.status = d.status;
         l.wait_budget = g_wait_budget.load();
         l.fault_skip_kblock = g_fault_skip_kblock.load();
-        cudaError_t err = tc_gemm_launch(l, stream);
+        cudaError_t err = (kernel == GEMM_KERNEL_TC_SMALL) ? tc_small_launch(l, stream)
+                                                            : tc_gemm_launch(l, stream);
         if (err == cudaErrorNotSupported)
             return GEMM_ERR_UNSUPPORTED;
         return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -336,17 +362,17 @@ namespace {
 
 // K ranges gemm_ex_ws splits a product with few output tiles into: when the
 // 128 x 128 tiles would occupy at most a quarter of the SMs and K holds at
-// least eight 64-wide steps, K is divided so that up to one unit of work runs
-// per SM, at most 8 ranges.  0 = no split.  Eight rather than more: measured
-// on GB300 (BF16, L2 flushed between calls), 96 x 200 x 1000 took 11.9 us
-// with 8 ranges against 12.3 us with 16, 128 x 128 x 2048 12.3 against
-// 12.7 us, 256 x 256 x 4096 12.7 against 12.9 us; the extra partials cost
-// more in the reduction than the shorter ranges save.
+// least kSplitMinKBlocks 64-wide steps, K is divided so that up to one unit
+// of work runs per SM, at most 8 ranges.  0 = no split.  Eight rather than
+// more: measured on GB300 (BF16, L2 flushed between calls), 128 x 128 x
+// 2048 took 12.3 us with 8 ranges against 12.7 us with 16, 256 x 256 x 4096
+// 12.7 against 12.9 us; the extra partials cost more in the reduction than
+// the shorter ranges save.
 int few_tile_splits(int64_t M, int64_t N, int64_t K, int num_sms)
 {
     const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
     const int64_t k_blocks = (K + 63) / 64;
-    if (tiles <= 0 || tiles * 4 > num_sms || k_blocks < 8)
+    if (tiles <= 0 || tiles * 4 > num_sms || k_blocks < kSplitMinKBlocks)
         return 0;
     const int64_t s = std::min<int64_t>(std::min<int64_t>(num_sms / tiles, k_blocks), 8);
     if (s < 2)

@@ -15,7 +15,7 @@ void note_launch();
 enum { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 
 // Tensor-core kernel variants; they match the gemm_kernel_t values.
-enum { TC_128x128 = 3, TC_128x256 = 4, TC_256x256 = 5, TC_256x128 = 6 };
+enum { TC_128x128 = 3, TC_128x256 = 4, TC_256x256 = 5, TC_256x128 = 6, TC_SMALL = 7 };
 
 // Whether a variant runs on CTA pairs (cta_group::2).
 inline bool tc_is_pair(int variant) { return variant == TC_256x256 || variant == TC_256x128; }
@@ -96,6 +96,11 @@ cudaError_t tc_hybrid_launch(const TcLaunch& l, cudaStream_t stream);
 // Sums the split partials of the tail tiles described by plan[] (as filled
 // by the tensor-core launch) into C, applying alpha and beta.
 cudaError_t tail_reduce_launch(const TcLaunch& l, const int* plan, cudaStream_t stream);
+
+// The single-tile kernel for products whose 128-row tiles fit in one wave
+// of CTAs (tc_small.cu): one CTA per 128 x tc_small_tile_n() output tile.
+cudaError_t tc_small_launch(const TcLaunch& l, cudaStream_t stream);
+int tc_small_tile_n(int64_t M, int64_t N, int num_sms);
 
 // Encodes the tensor maps and launches; returns cudaSuccess, a CUDA error, or
 // cudaErrorNotSupported when the driver entry point for tensor maps is
