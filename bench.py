@@ -461,6 +461,16 @@ def link_rates(host_in, dev_in, dev_out, host_out, stream, reps=5):
 SMALL_WORKLOADS = ("worked_9x9", "square_128_f16", "edge_96x200x1000_bf16")
 
 
+def trimmed_mean(xs, cut=0.1):
+    """Mean of the middle (1 - 2 cut) of the values: event times of a few
+    microseconds come in steps of about half a microsecond, so a median
+    jumps between steps where a trimmed mean does not."""
+    v = sorted(xs)
+    k = int(len(v) * cut)
+    v = v[k:len(v) - k] or v
+    return sum(v) / len(v)
+
+
 def oracle_seconds(A, B, threads, min_seconds=0.2, min_reps=3):
     """Median wall time of one full oracle product on `threads` threads."""
     import oracle
@@ -477,9 +487,9 @@ def oracle_seconds(A, B, threads, min_seconds=0.2, min_reps=3):
 
 def small_workload_lines(dev, flush_buf_bytes):
     """For each small named workload: the GPU time of the benchmarked call
-    (gemm_ex_ws, automatic choice; median of 200 steps with L2 overwritten
-    between them), cuBLAS on the same 16-bit inputs, and the full CPU
-    oracle product on all host cores and on one thread."""
+    (gemm_ex_ws, automatic choice; median and trimmed mean of 400 steps with
+    L2 overwritten between them), cuBLAS on the same 16-bit inputs, and the
+    full CPU oracle product on all host cores and on one thread."""
     import torch
     import oracle
     import tiled_matrix_multiplication_output_gb300 as tg
@@ -506,17 +516,19 @@ def small_workload_lines(dev, flush_buf_bytes):
 
         for _ in range(5):
             step()
-        _, per = timed_loop(step, 200, stream, flush)
+        _, per = timed_loop(step, 400, stream, flush)
         gpu_us = statistics.median(per) * 1e3
+        gpu_us_mean = trimmed_mean(per) * 1e3
         line = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "in_dtype": w.in_dtype,
-                "out_dtype": w.out_dtype, "gpu_us": gpu_us,
+                "out_dtype": w.out_dtype, "gpu_us": gpu_us, "gpu_us_trimmed_mean": gpu_us_mean,
                 "gpu_tflops": w.flops / (gpu_us * 1e-6) / 1e12,
                 "gpu_gbs_compulsory": footprint_bytes(w) / (gpu_us * 1e-6) / 1e9}
         if w.in_dtype != "f32":
             for _ in range(5):
                 torch.matmul(A, B)
-            _, per = timed_loop(lambda: torch.matmul(A, B), 200, stream, flush)
+            _, per = timed_loop(lambda: torch.matmul(A, B), 400, stream, flush)
             line["cublas_us"] = statistics.median(per) * 1e3
+            line["cublas_us_trimmed_mean"] = trimmed_mean(per) * 1e3
         cpu = {}
         for label, nthr in (("all_cores", threads), ("one_thread", 1)):
             sec = oracle_seconds(A_cpu, B_cpu, nthr)

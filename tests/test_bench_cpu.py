@@ -161,3 +161,8 @@ def test_roofline_carries_the_theoretical_tensor_peak():
     small = inputs.WORKLOADS["square_128_f16"]
     assert "theoretical_peak" not in bench.roofline_of(small, _flops(small), 0.01, PEAKS,
                                                         "measured", None)
+
+
+def test_trimmed_mean_drops_the_tails():
+    assert bench.trimmed_mean([1.0] * 8 + [100.0, -50.0]) == pytest.approx(1.0)
+    assert bench.trimmed_mean([2.0, 4.0]) == pytest.approx(3.0)
