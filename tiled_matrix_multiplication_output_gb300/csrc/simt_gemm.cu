@@ -307,9 +307,10 @@ __global__ void __launch_bounds__(256, 2)
         // tile.  The previous output tile's last barrier follows all of its
         // shared-memory reads, so both buffers are free here.  Two schedules
         // of the register prefetch, chosen per operand layout by measurement
-        // (FP32 4096^3 on GB300: one tile ahead 48.5 / 46.6 / 48.8 TFLOP/s
-        // for A, B as stored / B transposed / both transposed, two tiles
-        // ahead 45.3 against 40.3 for A transposed with B as stored):
+        // on GB300 (one tile ahead was the faster on three layouts, two
+        // ahead on A transposed with B as stored, by about 12 %; measured
+        // with FP32 operands, which now go to simt_gemm_f32v_kernel when
+        // their rows are 16-byte aligned):
         //  - one ahead: tile t + 1 is loaded before the multiplies of tile t
         //    and stored into the other buffer after them;
         //  - two ahead: tile t + 1, loaded during iteration t - 1, is stored
