@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustained-seconds", type=float, default=2.5,
+                    help="step time of the sustained leg after the timed region (0: none)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark line: time every tensor-core variant, the "
                          "automatic choice and cuBLAS on a fixed list of BF16 shapes, one JSON "
@@ -623,11 +625,14 @@ def run_ours(args, rank, world, local):
         return
 
     # ---- the same step held for seconds: the power-capped rate
-    sus_steps, sus_ms, sus_clocks = sustained_leg(step, ms_per_step, stream, flush_buf, local)
-    sus_ms = max_over_ranks(sus_ms, world)
-    sustained = {"value": job_rate(flops, sus_steps, world, sus_ms), "unit": UNIT,
-                 "steps": sus_steps, "ms_per_step": sus_ms / sus_steps,
-                 "seconds": sus_ms * 1e-3, "clocks": sus_clocks}
+    sustained = None
+    if args.sustained_seconds > 0:
+        sus_steps, sus_ms, sus_clocks = sustained_leg(step, ms_per_step, stream, flush_buf, local,
+                                                      seconds=args.sustained_seconds)
+        sus_ms = max_over_ranks(sus_ms, world)
+        sustained = {"value": job_rate(flops, sus_steps, world, sus_ms), "unit": UNIT,
+                     "steps": sus_steps, "ms_per_step": sus_ms / sus_steps,
+                     "seconds": sus_ms * 1e-3, "clocks": sus_clocks}
 
     # ---- end to end through the host-buffer entry point
     in_b = 4 if w.in_dtype == "f32" else 2
@@ -674,9 +679,12 @@ def run_ours(args, rank, world, local):
     n_cublas = args.steps   # same length as our timed loop
     cublas_ms, _ = timed_loop(lambda: torch.matmul(A, B), n_cublas, stream, flush_buf)
     cublas_tflops = flops * n_cublas / (cublas_ms * 1e-3) / 1e12
-    cb_steps, cb_ms, cb_clocks = sustained_leg(lambda: torch.matmul(A, B), cublas_ms / n_cublas,
-                                               stream, flush_buf, local)
-    cublas_sustained = flops * cb_steps / (cb_ms * 1e-3) / 1e12
+    cublas_sustained, cb_clocks = None, None
+    if args.sustained_seconds > 0:
+        cb_steps, cb_ms, cb_clocks = sustained_leg(lambda: torch.matmul(A, B), cublas_ms / n_cublas,
+                                                   stream, flush_buf, local,
+                                                   seconds=args.sustained_seconds)
+        cublas_sustained = flops * cb_steps / (cb_ms * 1e-3) / 1e12
 
     if rank != 0:
         return
@@ -688,12 +696,12 @@ def run_ours(args, rank, world, local):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     roofline = roofline_of(w, flops, avg_launch_ms, peaks, peak_kind, traffic, sms=sms,
                            run_mhz=(clocks or {}).get("sm_mhz"))
-    if roofline["bound"] == "tensor":
+    if roofline["bound"] == "tensor" and sustained:
         sustained["frac_of_sustained_peak"] = sustained["value"] / float(
             peaks["bf16_tflops_sustained"])
-        if sus_clocks and sus_clocks.get("sm_mhz"):
+        if sustained["clocks"] and sustained["clocks"].get("sm_mhz"):
             sustained["frac_of_theoretical_at_run_clock"] = sustained["value"] / (
-                theoretical_tensor_tflops(sms, sus_clocks["sm_mhz"]) * world)
+                theoretical_tensor_tflops(sms, sustained["clocks"]["sm_mhz"]) * world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
