@@ -381,12 +381,18 @@ __global__ void __launch_bounds__(256, 2)
 // multiple of 4): the large-tile kernel with 16-byte global loads.  A
 // 128 x 128 block tile, K tiles of 16, an 8 x 8 micro-tile per thread laid
 // out as in simt_gemm_big_kernel.  Each thread moves two 16-byte words of
-// each operand per K tile; words that run along k in memory (A as stored, B
-// transposed) are scattered into the K-major shared tile as four 4-byte
-// stores, words that run along m or n (A transposed, B as stored) land as
-// one 16-byte store.  With K % 4 == 0 (or M, N % 4 == 0 for the transposed
-// forms) a word is either wholly inside the matrix or wholly outside it, so
-// one guard per word keeps ragged edges exact.
+// each operand per K tile.  Words that run along m or n in memory (A
+// transposed, B as stored) land whole in the K-major shared tile and are
+// copied there by cp.async, without passing through registers; words that
+// run along k (A as stored, B transposed) are loaded into registers one K
+// tile ahead and scattered as four 4-byte stores.  With K % 4 == 0 (or M,
+// N % 4 == 0 for the transposed forms) a word is either wholly inside the
+// matrix or wholly outside it, so one guard per word keeps ragged edges
+// exact (cp.async reads nothing and writes zeros for a word outside).
+//
+// Measured on GB300 (FP32 4096^3, TFLOP/s, cp.async / register staging for
+// the words that land whole): A, B as stored 59.2 / 56.6; A transposed
+// 62.0 / 54.9; B transposed and both transposed unchanged (57.0, 54.8).
 //
 // With B as stored, the multiply-adds run in pairs: fma.rn.f32x2 performs
 // two IEEE single-precision fused multiply-adds (columns 2p and 2p + 1 of a
@@ -404,6 +410,11 @@ __global__ void __launch_bounds__(256, 2)
 {
     constexpr int BM = 128, BN = 128, BK = 16, NT = 256, LD = BM + 4;
     constexpr bool PAIRED = !OP_B;
+    // Operands whose 16-byte words run along m or n in memory (A
+    // transposed, B as stored) go global -> shared by cp.async; the others
+    // are staged through registers and scattered into the K-major tile.
+    constexpr bool ASYNC_A = OP_A, ASYNC_B = !OP_B;
+    constexpr bool ASYNC = ASYNC_A || ASYNC_B;
     // words per thread per operand and K tile: BM * BK / 4 / NT
     constexpr int WA = BM * BK / 4 / NT, WB = BK * BN / 4 / NT;
     __shared__ __align__(16) float As3[2][BK][LD];
@@ -411,9 +422,10 @@ __global__ void __launch_bounds__(256, 2)
     // Shared-memory addresses are spelled two ways below, which give the
     // same addresses but lead the compiler to different schedules: array
     // subscripts in the paired form, a flat offset (these lambdas) in the
-    // single one.  Measured on GB300 (FP32 4096^3, TFLOP/s): subscripts
-    // 56.6 against 53.0 with A and B as stored; the flat offset 56.6 against
-    // 55.2 with B transposed and 54.9 against 52.9 with both transposed.
+    // single one.  Measured on GB300 (FP32 4096^3, TFLOP/s, with every
+    // operand staged through registers): subscripts 56.6 against 53.0 with
+    // A and B as stored; the flat offset 56.6 against 55.2 with B
+    // transposed and 54.9 against 52.9 with both transposed.
     auto As = [&](int buf, int k, int m) -> float* { return &As3[0][0][0] + (buf * BK + k) * LD + m; };
     auto Bs = [&](int buf, int k, int n) -> float* { return &Bs3[0][0][0] + (buf * BK + k) * LD + n; };
 
@@ -476,23 +488,51 @@ __global__ void __launch_bounds__(256, 2)
     auto load_tile = [&](int k0) {
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < WA; ++w) {
+        for (int w = 0; w < WA && !ASYNC_A; ++w) {
             const int kk = OP_A ? k0 + a_r + w * A_DR : k0 + a_c;
             ra[w] = ((a_ok >> w) & 1u) && kk < K
                         ? __ldg(reinterpret_cast<const float4*>(a_ptr + w * a_wstride))
                         : z;
         }
 #pragma unroll
-        for (int w = 0; w < WB; ++w) {
+        for (int w = 0; w < WB && !ASYNC_B; ++w) {
             const int kk = OP_B ? k0 + b_c : k0 + b_r + w * B_DR;
             rb[w] = ((b_ok >> w) & 1u) && kk < K
                         ? __ldg(reinterpret_cast<const float4*>(b_ptr + w * b_wstride))
                         : z;
         }
     };
+    // Operands whose 16-byte words land whole in the shared tile (A
+    // transposed, B as stored), copied global -> shared without registers
+    // (cp.async, 16 bytes, zero fill past the edges).
+    auto copy_async = [&](int buf, int k0) {
+#pragma unroll
+        for (int w = 0; w < WA && ASYNC_A; ++w) {
+            const int kk = k0 + a_r + w * A_DR;
+            const bool in = ((a_ok >> w) & 1u) && kk < K;
+            const float* src = in ? a_ptr + w * a_wstride : A;
+            const uint32_t dst = static_cast<uint32_t>(
+                __cvta_generic_to_shared(&As3[buf][a_r + w * A_DR][a_c]));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                         "r"(in ? 16 : 0)
+                         : "memory");
+        }
+#pragma unroll
+        for (int w = 0; w < WB && ASYNC_B; ++w) {
+            const int kk = k0 + b_r + w * B_DR;
+            const bool in = ((b_ok >> w) & 1u) && kk < K;
+            const float* src = in ? b_ptr + w * b_wstride : B;
+            const uint32_t dst = static_cast<uint32_t>(
+                __cvta_generic_to_shared(&Bs3[buf][b_r + w * B_DR][b_c]));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                         "r"(in ? 16 : 0)
+                         : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
     auto store_tile = [&](int buf) {
 #pragma unroll
-        for (int w = 0; w < WA; ++w) {
+        for (int w = 0; w < WA && !ASYNC_A; ++w) {
             if constexpr (PAIRED) {
                 if (OP_A) {
                     *reinterpret_cast<float4*>(&As3[buf][a_r + w * A_DR][a_c]) = ra[w];
@@ -514,7 +554,7 @@ __global__ void __launch_bounds__(256, 2)
             }
         }
 #pragma unroll
-        for (int w = 0; w < WB; ++w) {
+        for (int w = 0; w < WB && !ASYNC_B; ++w) {
             if (OP_B) {
                 const int r = b_r + w * B_DR;
                 *Bs(buf, b_c + 0, r) = rb[w].x;
@@ -593,8 +633,12 @@ __global__ void __launch_bounds__(256, 2)
         set_tile(m0, n0);
         const int nk = (K + BK - 1) / BK;
         if (nk > 0) {
+            if constexpr (ASYNC)
+                copy_async(0, 0);
             load_tile(0);
             store_tile(0);
+            if constexpr (ASYNC)
+                asm volatile("cp.async.wait_all;" ::: "memory");
             __syncthreads();
         }
         for (int t = 0; t < nk; ++t) {
@@ -602,11 +646,15 @@ __global__ void __launch_bounds__(256, 2)
             if (more) {
                 a_ptr += a_kstep;
                 b_ptr += b_kstep;
+                if constexpr (ASYNC)
+                    copy_async((t + 1) & 1, (t + 1) * BK);
                 load_tile((t + 1) * BK);
             }
             multiply(t & 1);
             if (more)
                 store_tile((t + 1) & 1);
+            if constexpr (ASYNC)
+                asm volatile("cp.async.wait_all;" ::: "memory");
             __syncthreads();
         }
 
