@@ -394,22 +394,24 @@ __global__ void __launch_bounds__(256, 2)
 // the words that land whole): A, B as stored 59.2 / 56.6; A transposed
 // 62.0 / 54.9; B transposed and both transposed unchanged (57.0, 54.8).
 //
-// With B as stored, the multiply-adds run in pairs: fma.rn.f32x2 performs
-// two IEEE single-precision fused multiply-adds (columns 2p and 2p + 1 of a
-// micro-tile row) in one instruction, so a K step issues 32 instructions
-// for its 64 multiply-adds and leaves issue slots for the fragment loads.
-// Each result is the same fused multiply-add as fmaf, in the same order.
-// Measured on GB300 (FP32, 4096^3, TFLOP/s, paired / single): A and B as
-// stored 56.7 / 50.3, A transposed 55.8 / 51.0; with B transposed the
-// paired form needs more registers than two blocks per SM leave and lost
-// (52.8 / 55.1, 51.5 / 52.9), so those layouts issue single FMAs.
+// The multiply-adds run in pairs (fma.rn.f32x2: two IEEE single-precision
+// fused multiply-adds, columns 2p and 2p + 1 of a micro-tile row, in one
+// instruction), so a K step issues 32 instructions for its 64 multiply-adds
+// and leaves issue slots for the fragment loads; each result is the same
+// fused multiply-add as fmaf, in the same order.  The one exception is A as
+// stored with B transposed: both operands then go through registers, the
+// pairs' extra registers spill, and single FMAs are faster.  Measured on
+// GB300 (FP32 4096^3, TFLOP/s, paired / single), with every operand staged
+// through registers: A, B as stored 56.7 / 50.3; A transposed 55.8 / 51.0;
+// A as stored, B transposed 52.8 / 57.1.  Both transposed, with A copied by
+// cp.async: 58.5 / 54.8.
 template <typename OutT, bool OP_A, bool OP_B>
 __global__ void __launch_bounds__(256, 2)
     simt_gemm_f32v_kernel(const float* __restrict__ A, const float* __restrict__ B, OutT* C,
                           int M, int N, int K, float alpha, float beta)
 {
     constexpr int BM = 128, BN = 128, BK = 16, NT = 256, LD = BM + 4;
-    constexpr bool PAIRED = !OP_B;
+    constexpr bool PAIRED = !OP_B || OP_A;
     // Operands whose 16-byte words run along m or n in memory (A
     // transposed, B as stored) go global -> shared by cp.async; the others
     // are staged through registers and scattered into the K-major tile.
