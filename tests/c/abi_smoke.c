@@ -2,10 +2,11 @@
  * C-only check of the library's C ABI (include/tiled_gemm.h): no Python.
  *
  * Fills A (M x K) and B (K x N) with small integers in BF16, multiplies them
- * on the GPU through gemm (FP32 out), gemm_ex (BF16 out) and gemm_general
- * (C = 2 A^T B + C with A stored K x M), and compares every element with a
- * plain integer loop on the host: the products are exact, so equality is
- * required.  Exit status 0 on success; 1 on a mismatch; 2 on an API error;
+ * on the GPU through gemm (FP32 out), gemm_ex (BF16 out), gemm_general
+ * (C = 2 A^T B + C with A stored K x M), gemm_ex_kernel with the single-tile
+ * kernel and gemm_ex_host_ws (host buffers in and out), and compares every
+ * element with a plain integer loop on the host: the products are exact, so
+ * equality is required.  Exit status 0 on success; 1 on a mismatch; 2 on an API error;
  * 77 when no CUDA device is present.
  */
 #include <stdint.h>
@@ -120,8 +121,33 @@ int main(void)
     CUDA_CHECK(cudaMemcpy(c32, dC, 4 * M * N, cudaMemcpyDeviceToHost));
     for (int64_t i = 0; i < M * N; ++i)
         bad += c32[i] != (float)(2 * ref[i]) + cin[i];
+    /* the single-tile kernel, forced */
+    CHECK(gemm_ex_kernel(dA, dB, dC, M, N, K, GEMM_BF16, GEMM_F32, GEMM_F32, GEMM_KERNEL_TC_SMALL,
+                         NULL));
+    CHECK(gemm_device_status(NULL));
+    CUDA_CHECK(cudaMemcpy(c32, dC, 4 * M * N, cudaMemcpyDeviceToHost));
+    for (int64_t i = 0; i < M * N; ++i)
+        bad += c32[i] != (float)ref[i];
+    /* host buffers in and out, through the workspace form of the host path */
+    {
+        const size_t ws_bytes = gemm_workspace_size(M, N, K);
+        void* ws = NULL;
+        CUDA_CHECK(cudaMalloc(&ws, ws_bytes > 0 ? ws_bytes : 16));
+        memset(c32, 0, 4 * M * N);
+        CHECK(gemm_ex_host_ws(a, b, c32, M, N, K, GEMM_BF16, GEMM_F32, GEMM_F32, dA, dB, dC, ws,
+                              ws_bytes, NULL));
+        CUDA_CHECK(cudaDeviceSynchronize());
+        CHECK(gemm_device_status(NULL));
+        for (int64_t i = 0; i < M * N; ++i)
+            bad += c32[i] != (float)ref[i];
+        cudaFree(ws);
+    }
+    if (gemm_host_panel_rows(M) != M || gemm_host_panel_rows(8192) != 1024)
+        bad += 1;
     /* argument errors come back as codes */
     if (gemm(dA, dB, NULL, M, N, K, GEMM_BF16, GEMM_F32, NULL) != GEMM_ERR_INVALID_VALUE)
+        bad += 1;
+    if (gemm(dA, dB, dC, GEMM_MAX_DIM + 1, N, K, GEMM_BF16, GEMM_F32, NULL) != GEMM_ERR_INVALID_VALUE)
         bad += 1;
 
     cudaFree(dA);
