@@ -539,3 +539,20 @@ def test_simt_f32_wide_load_kernel_outputs_and_addmm():
     # random FP32 inputs: within the stated bound
     A, B = inputs.draw(M, N, 1000, "f32", "normal", seed=98)
     expect_close(run_gpu(A, B, torch.float32, "simt"), A, B)
+
+
+def test_large_products_with_k0_write_zeros_or_beta_c():
+    """K = 0 on the large-tile SIMT kernels (FP32 with aligned rows, and BF16
+    with an odd pitch) and on the tensor-core path's automatic choice: C =
+    beta * C_in, zeros for beta = 0."""
+    for dt in (torch.float32, torch.bfloat16):
+        A = torch.zeros(2048, 0, dtype=dt, device="cuda")
+        B = torch.zeros(0, 2052, dtype=dt, device="cuda")
+        out = torch.full((2048, 2052), 7.0, device="cuda")
+        tg.matmul(A, B, out=out, kernel="simt")
+        torch.cuda.synchronize()
+        assert not out.any()
+        C_in = torch.full((2048, 2052), 3.0, device="cuda")
+        tg.addmm(A, B, C_in, alpha=2.0, beta=-1.0, kernel="simt")
+        torch.cuda.synchronize()
+        assert torch.all(C_in == -3.0)
