@@ -79,9 +79,12 @@ typedef enum {
     GEMM_KERNEL_TC_128x256 = 4,/* tcgen05, one CTA per 128 x 256 output tile */
     GEMM_KERNEL_TC_256x256 = 5,/* tcgen05 cta_group::2, one CTA pair per 256 x 256 tile */
     GEMM_KERNEL_TC_256x128 = 6,/* tcgen05 cta_group::2, one CTA pair per 256 x 128 tile */
-    GEMM_KERNEL_TC_SMALL = 7   /* tcgen05, one CTA per 128 x 64 or 128 x 128 tile, not
+    GEMM_KERNEL_TC_SMALL = 7,  /* tcgen05, one CTA per 128 x 64 or 128 x 128 tile, not
                                   persistent: the lowest fixed cost, for products whose
                                   tiles fit in one wave */
+    GEMM_KERNEL_SIMT_SMALL = 8 /* FFMA, one 16 x 16 tile per thread block with its whole K
+                                  range copied at once and split between the block's warps:
+                                  the lowest latency, for small products */
 } gemm_kernel_t;
 
 /*
@@ -121,9 +124,14 @@ int gemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t
  * The tensor-core kernels need 16-bit inputs, 16-byte aligned A, B and C and
  * row pitches (K and N elements of the input type, N of the output type) that
  * are multiples of 16 bytes; a forced tensor-core kernel whose rules the
- * operands break returns GEMM_ERR_UNSUPPORTED.  The SIMT kernels take any
- * shape and any element-aligned pointer.  All kernels give results within
- * the same accuracy bound; they differ in the order of the K summation.
+ * operands break returns GEMM_ERR_UNSUPPORTED.  GEMM_KERNEL_SIMT and
+ * GEMM_KERNEL_SIMT_TPB3 take any shape and any element-aligned pointer.
+ * GEMM_KERNEL_SIMT_SMALL takes any type, 16-byte aligned A and B whose row
+ * pitches as stored are multiples of 16 bytes, and a K whose slices of one
+ * 16 x 16 tile fit in a block's shared memory (K up to about 3,400 for
+ * 16-bit inputs, 1,700 for FP32); otherwise it returns
+ * GEMM_ERR_UNSUPPORTED.  All kernels give results within the same accuracy
+ * bound; they differ in the order of the K summation.
  */
 int gemm_ex_kernel(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                    gemm_dtype_t in_dtype, gemm_dtype_t acc_dtype, gemm_dtype_t out_dtype,

@@ -2,6 +2,7 @@
 every function include/tiled_gemm.h declares, and rejects bad arguments on the
 host before touching a device."""
 import ctypes
+import re
 
 import pytest
 
@@ -122,3 +123,7 @@ def test_header_constants_match_the_binding():
     text = open(tg.binding.HEADER).read()
     assert "#define GEMM_MAX_DIM ((int64_t)2147483392)" in text
     assert 2147483392 == tg.binding.MAX_DIM
+    # every gemm_kernel_t value, by name, is the binding's kernel code
+    kernels = {m.group(1).lower(): int(m.group(2))
+               for m in re.finditer(r"GEMM_KERNEL_(\w+)\s*=\s*(\d+)", text)}
+    assert kernels == tg.KERNELS

@@ -137,15 +137,56 @@ bool small_kernel_fits(int64_t M, int64_t N, int64_t K, int num_sms)
     return tiles <= num_sms && (K + 63) / 64 < kSplitMinKBlocks;
 }
 
-// The automatic choice.  Tiny products go to the SIMT kernel (a tensor-core
-// launch has a fixed set-up cost); otherwise the tensor-core variant with the
+// Whether the latency-path SIMT kernel (simt_small.cu) takes a product.
+// Its 16 x 16 tiles each get a block of their own with the tile's whole K
+// range copied at once, so it is the fastest path while those tiles fit on
+// the SMs in one wave and K is short; for operands the tensor-core kernels
+// cannot take (FP32, or unaligned 16-bit pitches) it also beats the 64 x 64
+// SIMT kernel up to about eight tiles per SM.  Measured on GB300, L2
+// overwritten between calls, microseconds (this kernel / the previous
+// choice / cuBLAS): 128^3 F16 -> F32 6.3-7.0 / 7.9-8.3 (tc_small) /
+// 6.1-6.5; 96 x 200 x 1000 BF16 -> F32 9.7-10.3 / 11.0-11.3 / 8.4;
+// 160 x 160 x 640 BF16 8.4-8.7 / 9.1-9.7; 256^3 BF16 8.4-8.7 / 8.2-8.6
+// (two tiles per SM: not taken); FP32 128^3 7.1 / 12.6 (SIMT) / 9.9;
+// FP32 100 x 200 x 1000 12.6 / 58.0 / 19.0; FP32 512^3 22.4 / 33.4 / 18.6;
+// FP32 768^3 63.8 / 46.9 (nine tiles per SM: not taken).
+bool simt_small_takes(const Problem& q, bool tensor_ok, int num_sms)
+{
+    SimtLaunch l{};
+    l.in_dtype = q.in_dtype;
+    l.out_dtype = q.out_dtype;
+    l.op_a = q.op_a;
+    l.op_b = q.op_b;
+    l.A = q.A;
+    l.B = q.B;
+    l.C = q.C;
+    if (q.M > GEMM_MAX_DIM || q.N > GEMM_MAX_DIM || q.K > GEMM_MAX_DIM)
+        return false;
+    l.M = static_cast<int>(q.M);
+    l.N = static_cast<int>(q.N);
+    l.K = static_cast<int>(q.K);
+    l.num_sms = num_sms;
+    if (!simt_small_fits(l))
+        return false;
+    const int64_t tiles = ((q.M + 15) / 16) * ((q.N + 15) / 16);
+    if (tensor_ok)
+        return tiles <= num_sms && q.K <= 1024;
+    return tiles <= int64_t(8) * num_sms;
+}
+
+// The automatic choice.  Small products go to the latency-path SIMT kernel
+// (simt_small_takes); other operands the tensor-core kernels cannot take go
+// to the tiled SIMT kernel; otherwise the tensor-core variant with the
 // smallest predicted time: the tile traffic of the loop nest, the waves of
 // tiles over the resident CTAs and each tile shape's measured throughput
 // (predict_seconds in model.cu).
 int auto_kernel(const Problem& q, int num_sms)
 {
     const int64_t M = q.M, N = q.N, K = q.K;
-    if (!tc_eligible(q))
+    const bool tensor_ok = tc_eligible(q);
+    if (simt_small_takes(q, tensor_ok, num_sms))
+        return GEMM_KERNEL_SIMT_SMALL;
+    if (!tensor_ok)
         return GEMM_KERNEL_SIMT;
     const double flops = 2.0 * double(M) * double(N) * double(K);
     if (flops < 2.0 * 64 * 64 * 64)
@@ -172,6 +213,11 @@ int auto_kernel(const Problem& q, int num_sms)
     return best;
 }
 
+bool is_tc(int kernel)
+{
+    return kernel >= GEMM_KERNEL_TC_128x128 && kernel <= GEMM_KERNEL_TC_SMALL;
+}
+
 int validate_problem(const Problem& q)
 {
     int rc = validate(q.A, q.B, q.C, q.M, q.N, q.K, q.in_dtype, q.acc_dtype, q.out_dtype);
@@ -187,7 +233,7 @@ int run(const Problem& q, int kernel, cudaStream_t stream)
     int rc = validate_problem(q);
     if (rc != GEMM_OK)
         return rc;
-    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_TC_SMALL)
+    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_SIMT_SMALL)
         return GEMM_ERR_INVALID_VALUE;
     if (q.M == 0 || q.N == 0)
         return GEMM_OK;
@@ -196,7 +242,7 @@ int run(const Problem& q, int kernel, cudaStream_t stream)
         return GEMM_ERR_CUDA;
     if (kernel == GEMM_KERNEL_AUTO)
         kernel = auto_kernel(q, d.num_sms);
-    if (kernel >= GEMM_KERNEL_TC_128x128) {
+    if (is_tc(kernel)) {
         if (!tc_eligible(q))
             return GEMM_ERR_UNSUPPORTED;
         TcLaunch l{};
@@ -238,7 +284,10 @@ int run(const Problem& q, int kernel, cudaStream_t stream)
     l.N = static_cast<int>(q.N);
     l.K = static_cast<int>(q.K);
     l.num_sms = d.num_sms;
-    cudaError_t err = simt_gemm_launch(l, stream);
+    cudaError_t err = (kernel == GEMM_KERNEL_SIMT_SMALL) ? simt_small_launch(l, stream)
+                                                         : simt_gemm_launch(l, stream);
+    if (err == cudaErrorNotSupported)
+        return GEMM_ERR_UNSUPPORTED;
     return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -418,7 +467,7 @@ extern "C" int gemm_ws_split_count(int64_t M, int64_t N, int64_t K, gemm_dtype_t
     DeviceInfo d;
     if (device_info(&d) != cudaSuccess)
         return -GEMM_ERR_CUDA;
-    if (auto_kernel(q, d.num_sms) < GEMM_KERNEL_TC_128x128)
+    if (!is_tc(auto_kernel(q, d.num_sms)))
         return 0;
     return few_tile_splits(M, N, K, d.num_sms);
 }
@@ -440,7 +489,7 @@ extern "C" int gemm_ex_ws(const void* A, const void* B, void* C, int64_t M, int6
     if (device_info(&d) != cudaSuccess)
         return GEMM_ERR_CUDA;
     const int kernel = auto_kernel(q, d.num_sms);
-    if (workspace && kernel >= GEMM_KERNEL_TC_128x128) {
+    if (workspace && is_tc(kernel)) {
         // Few output tiles and a long K: split K across the idle SMs.
         const int splits = few_tile_splits(M, N, K, d.num_sms);
         if (splits > 1 && workspace_bytes >= gemm_splitk_workspace_size(M, N, K, splits))
