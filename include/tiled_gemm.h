@@ -82,9 +82,10 @@ typedef enum {
     GEMM_KERNEL_TC_SMALL = 7,  /* tcgen05, one CTA per 128 x 64 or 128 x 128 tile, not
                                   persistent: the lowest fixed cost, for products whose
                                   tiles fit in one wave */
-    GEMM_KERNEL_SIMT_SMALL = 8 /* FFMA, one 16 x 16 tile per thread block with its whole K
-                                  range copied at once and split between the block's warps:
-                                  the lowest latency, for small products */
+    GEMM_KERNEL_TILE16 = 8     /* one 16 x 16 tile per thread block with its whole K range
+                                  copied at once and split between the block's warps
+                                  (warp-level MMA for 16-bit inputs, FFMA for FP32): the
+                                  lowest latency, for small products */
 } gemm_kernel_t;
 
 /*
@@ -126,7 +127,7 @@ int gemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t
  * are multiples of 16 bytes; a forced tensor-core kernel whose rules the
  * operands break returns GEMM_ERR_UNSUPPORTED.  GEMM_KERNEL_SIMT and
  * GEMM_KERNEL_SIMT_TPB3 take any shape and any element-aligned pointer.
- * GEMM_KERNEL_SIMT_SMALL takes any type, 16-byte aligned A and B whose row
+ * GEMM_KERNEL_TILE16 takes any type, 16-byte aligned A and B whose row
  * pitches as stored are multiples of 16 bytes, and a K whose slices of one
  * 16 x 16 tile fit in a block's shared memory (K up to about 3,400 for
  * 16-bit inputs, 1,700 for FP32); otherwise it returns

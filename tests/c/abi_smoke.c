@@ -130,7 +130,7 @@ int main(void)
         bad += c32[i] != (float)ref[i];
     /* the latency-path SIMT kernel, forced */
     CHECK(gemm_ex_kernel(dA, dB, dC, M, N, K, GEMM_BF16, GEMM_F32, GEMM_F32,
-                         GEMM_KERNEL_SIMT_SMALL, NULL));
+                         GEMM_KERNEL_TILE16, NULL));
     CHECK(gemm_device_status(NULL));
     CUDA_CHECK(cudaMemcpy(c32, dC, 4 * M * N, cudaMemcpyDeviceToHost));
     for (int64_t i = 0; i < M * N; ++i)

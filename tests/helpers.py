@@ -9,9 +9,8 @@ import oracle
 import tiled_matrix_multiplication_output_gb300 as tg
 
 TC_KERNELS = ("tc_128x128", "tc_128x256", "tc_256x256", "tc_256x128", "tc_small")
-# simt_small needs 16-byte aligned operand rows; the other two take any shape.
-SIMT_KERNELS = ("simt", "simt_tpb3", "simt_small")
-ALL_KERNELS = SIMT_KERNELS + TC_KERNELS
+# tile16 needs 16-byte aligned operand rows; the two SIMT kernels take any shape.
+ALL_KERNELS = ("simt", "simt_tpb3", "tile16") + TC_KERNELS
 
 # Half an ulp at 1.0 of each output type: the relative size of one
 # round-to-nearest step when the FP32 accumulator is written out.  Used only

@@ -33,7 +33,7 @@ def test_bench_prints_one_complete_line():
     assert d["n_gpus"] == 1 and d["steps"] == 20 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0
     assert d["config"]["workload"] == "square_128_f16"
-    assert d["config"]["kernel"] == "simt_small"
+    assert d["config"]["kernel"] == "tile16"
     roof = d["roofline"]
     for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert key in roof, key

@@ -37,7 +37,7 @@ def _run(A, B, op_a, op_b, kernel, alpha=1.0, beta=0.0, C_in=None, out_dtype=tor
 
 
 @pytest.mark.parametrize("op_a,op_b", OPS)
-@pytest.mark.parametrize("kernel", TC_KERNELS + ("simt", "simt_small", "auto"))
+@pytest.mark.parametrize("kernel", TC_KERNELS + ("simt", "tile16", "auto"))
 def test_transposes_exact(op_a, op_b, kernel):
     """Integer inputs, several tiles with ragged edges (304 x 264 x 520: all
     pitches multiples of 8 so every layout is tensor-core eligible)."""
@@ -53,12 +53,12 @@ def test_transposes_random_tolerance(op_a, op_b):
     A0, B0 = inputs.draw(520, 392, 1032, "f16", "normal", seed=61)
     A, B = _stored(A0, B0, op_a, op_b)
     ref, Cabs = oracle.gemm_general(A, B, op_a, op_b)
-    for kernel in TC_KERNELS + ("simt", "simt_small"):
+    for kernel in TC_KERNELS + ("simt", "tile16"):
         for out in (torch.float32, torch.bfloat16):
             tolerance_check(_run(A, B, op_a, op_b, kernel, out_dtype=out), ref, Cabs)
 
 
-@pytest.mark.parametrize("kernel", TC_KERNELS + ("simt", "simt_tpb3", "simt_small"))
+@pytest.mark.parametrize("kernel", TC_KERNELS + ("simt", "simt_tpb3", "tile16"))
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
 def test_addmm_exact_integers(kernel, out_dtype):
     """alpha = 2, beta = -1 with integer C_in: exact in every output type
@@ -70,7 +70,7 @@ def test_addmm_exact_integers(kernel, out_dtype):
     np.testing.assert_array_equal(C.double().numpy(), oracle.round_to(ref, out_dtype).double().numpy())
 
 
-@pytest.mark.parametrize("kernel", TC_KERNELS + ("simt", "simt_small"))
+@pytest.mark.parametrize("kernel", TC_KERNELS + ("simt", "tile16"))
 def test_addmm_random_and_transposed(kernel):
     A0, B0 = inputs.draw(304, 264, 776, "bf16", "normal", seed=63)
     A, B = _stored(A0, B0, "t", "t")
@@ -85,7 +85,7 @@ def test_addmm_random_and_transposed(kernel):
 def test_beta_zero_ignores_nan_in_c():
     A0, B0 = inputs.draw(256, 256, 64, "bf16", "int", seed=64)
     C_in = torch.full((256, 256), float("nan"))
-    for kernel in TC_KERNELS + ("simt", "simt_small"):
+    for kernel in TC_KERNELS + ("simt", "tile16"):
         C = _run(A0, B0, "n", "n", kernel, beta=0.0, C_in=C_in)
         assert torch.isfinite(C).all()
 

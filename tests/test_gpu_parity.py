@@ -182,7 +182,7 @@ def test_large_k_and_many_tiles(kernel):
 # ---------------------------------------------------------- special cases
 
 def test_k0_writes_zeros():
-    for kernel in ("auto", "simt", "simt_small"):
+    for kernel in ("auto", "simt", "tile16"):
         A = torch.zeros(37, 0, dtype=torch.bfloat16, device="cuda")
         B = torch.zeros(0, 24, dtype=torch.bfloat16, device="cuda")
         out = torch.full((37, 24), 7.0, device="cuda")
@@ -203,18 +203,18 @@ def test_m0_n0_noop():
 def test_identity_and_gemv():
     A, _ = inputs.draw(256, 1, 256, "bf16", "normal", seed=10)
     eye = torch.eye(256, dtype=torch.bfloat16)
-    for kernel in TC_KERNELS + ("simt", "simt_small"):
+    for kernel in TC_KERNELS + ("simt", "tile16"):
         C = run_gpu(A, eye, torch.float32, kernel)
         assert torch.equal(C, A.float())
     # M = 1: a row vector times a matrix
     a, b = inputs.draw(1, 512, 384, "bf16", "normal", seed=11)
-    for kernel in TC_KERNELS + ("simt_small",):
+    for kernel in TC_KERNELS + ("tile16",):
         expect_close(run_gpu(a, b, torch.float32, kernel), a, b)
 
 
 def test_deterministic_run_to_run():
     A, B = inputs.draw(640, 768, 2048, "bf16", "normal", seed=12)
-    for kernel in TC_KERNELS + ("simt_small",):
+    for kernel in TC_KERNELS + ("tile16",):
         C1 = run_gpu(A, B, torch.bfloat16, kernel)
         C2 = run_gpu(A, B, torch.bfloat16, kernel)
         assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
@@ -340,9 +340,10 @@ def test_host_buffer_entry_point_with_workspace(M, N, K, out_dtype):
 
 
 def test_automatic_choice_on_the_named_workloads():
-    """The automatic picks on the named workloads: the latency-path SIMT
-    kernel when its 16 x 16 tiles fit in one wave and K is short (and for
-    aligned FP32 products of up to eight tiles per SM), the non-persistent
+    """The automatic picks on the named workloads: the latency-path kernel
+    when its 16 x 16 tiles' copies are short (one tile per SM up to K =
+    2048, or up to three per SM and 1024 x SMs tile-K values; aligned FP32
+    products of up to eight tiles per SM), the non-persistent
     single-tile kernel when 128 x 64 tiles fit in one wave, the CTA-pair
     kernel for the large squares, the tiled SIMT kernel for the rest of FP32
     and for shapes the tensor maps cannot take."""
@@ -353,11 +354,13 @@ def test_automatic_choice_on_the_named_workloads():
         return tg.KERNEL_NAMES[tg.gemm_select_kernel(A.data_ptr(), B.data_ptr(), C.data_ptr(),
                                                      M, N, K, in_dt, tg.F32, out_dt)]
     assert pick(9, 9, 9, tg.F32, tg.F32, torch.float32) == "simt"
-    assert pick(128, 128, 128, tg.F16, tg.F32, torch.float16) == "simt_small"
-    assert pick(96, 200, 1000, tg.BF16, tg.F32) == "simt_small"
-    assert pick(100, 200, 1000, tg.F32, tg.F32, torch.float32) == "simt_small"
+    assert pick(128, 128, 128, tg.F16, tg.F32, torch.float16) == "tile16"
+    assert pick(96, 200, 1000, tg.BF16, tg.F32) == "tile16"
+    assert pick(100, 200, 1000, tg.F32, tg.F32, torch.float32) == "tile16"
     assert pick(1024, 1024, 1024, tg.F32, tg.F32, torch.float32) == "simt"
-    assert pick(256, 256, 256, tg.BF16, tg.BF16) == "tc_small"
+    assert pick(256, 256, 256, tg.BF16, tg.BF16) == "tile16"      # two tiles per SM, short K
+    assert pick(128, 128, 2048, tg.BF16, tg.BF16) == "tile16"
+    assert pick(256, 256, 1024, tg.BF16, tg.BF16) == "tc_small"
     assert pick(512, 512, 512, tg.BF16, tg.BF16) == "tc_small"
     assert pick(256, 256, 4096, tg.BF16, tg.F32) == "tc_128x128"   # split along K by gemm_ex_ws
     assert pick(4096, 4096, 4096, tg.F16, tg.F16, torch.float16) == "tc_256x256"

@@ -81,7 +81,8 @@ def test_gemm_ex_ws_splits_few_tile_products():
     or more; 96 x 200 x 4000 here): two launches, bit for bit the result of
     gemm_splitk with the reported count, on integer and on random inputs;
     large products and shorter K are not split (the 96 x 200 x 1000
-    workload runs on one CTA per tile in a single launch)."""
+    workload, and up to K = 2048, run on the 16 x 16-tile kernel in a
+    single launch)."""
     M, N, K = 96, 200, 4000
     count = tg.gemm_ws_split_count(M, N, K, tg.BF16, tg.F32, tg.F32)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -89,7 +90,8 @@ def test_gemm_ex_ws_splits_few_tile_products():
     assert tg.gemm_ws_split_count(8192, 8192, 8192, tg.BF16, tg.F32, tg.BF16) == 0
     assert tg.gemm_ws_split_count(128, 128, 128, tg.F16, tg.F32, tg.F32) == 0
     assert tg.gemm_ws_split_count(96, 200, 1000, tg.BF16, tg.F32, tg.F32) == 0  # 16 K steps
-    assert tg.gemm_ws_split_count(96, 200, 2048, tg.BF16, tg.F32, tg.F32) >= 2  # 32 K steps
+    assert tg.gemm_ws_split_count(96, 200, 2048, tg.BF16, tg.F32, tg.F32) == 0  # tile16 (K <= 2048)
+    assert tg.gemm_ws_split_count(96, 200, 2056, tg.BF16, tg.F32, tg.F32) >= 2  # 33 K steps
     assert tg.gemm_ws_split_count(96, 200, 4000, tg.F32, tg.F32, tg.F32) == 0   # SIMT path
     assert tg.gemm_ws_split_count(-1, 200, 1000, tg.BF16, tg.F32, tg.F32) == -tg.binding.ERR_INVALID_VALUE
     A, B = inputs.draw(M, N, K, "bf16", "int", seed=31)

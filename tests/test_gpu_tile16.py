@@ -1,8 +1,8 @@
-"""The latency-path SIMT kernel (simt_small: one 16 x 16 output tile per
-block, the tile's whole K range copied at once and split between the
-block's eight warps) against the CPU oracle: bit-exact on integer inputs in
-every layout and type, within the stated bound on random ones, with its
-operand rules enforced."""
+"""The latency-path kernel (tile16: one 16 x 16 output tile per block, the
+tile's whole K range copied at once and split between the block's eight
+warps; warp-level MMA for 16-bit inputs, FFMA for FP32) against the CPU
+oracle: bit-exact on integer inputs in every layout and type, within the
+stated bound on random ones, with its operand rules enforced."""
 import itertools
 
 import numpy as np
@@ -39,14 +39,14 @@ def _stored(A0, B0, op_a, op_b):
 
 def _exact_batch(cases):
     """Each (M, N, K, in_dtype, out_dtype, op_a, op_b, seed) case launched on
-    simt_small before one synchronisation, then compared bit for bit with
+    tile16 before one synchronisation, then compared bit for bit with
     the oracle's exact product of the integer inputs."""
     runs = []
     for M, N, K, in_dt, out_dt, op_a, op_b, seed in cases:
         A0, B0 = inputs.draw(M, N, K, in_dt, "int", seed=seed)
         A, B = _stored(A0, B0, op_a, op_b)
         C = tg.addmm(A.cuda(), B.cuda(), op_a=op_a, op_b=op_b, out_dtype=out_dt,
-                     kernel="simt_small")
+                     kernel="tile16")
         runs.append((A, B, op_a, op_b, C))
     assert tg.gemm_device_status(torch.cuda.current_stream().cuda_stream) == tg.binding.OK
     for A, B, op_a, op_b, C in runs:
@@ -109,12 +109,12 @@ def test_longest_k_and_the_shared_memory_limit(in_dt, k_max, k_over):
     A = torch.zeros(40, k_over, dtype=tg.binding.torch_dtype(in_dt), device="cuda")
     B = torch.zeros(k_over, 24, dtype=A.dtype, device="cuda")
     with pytest.raises(tg.GemmError) as e:
-        tg.matmul(A, B, kernel="simt_small")
+        tg.matmul(A, B, kernel="tile16")
     assert e.value.code == tg.binding.ERR_UNSUPPORTED
     C = torch.empty(40, 24, device="cuda")
     k = tg.gemm_select_kernel(A.data_ptr(), B.data_ptr(), C.data_ptr(), 40, 24, k_over,
                               tg.binding.dtype_code(A.dtype), tg.F32, tg.F32)
-    assert tg.KERNEL_NAMES[k] != "simt_small"
+    assert tg.KERNEL_NAMES[k] != "tile16"
 
 
 def test_unaligned_operands_are_refused():
@@ -123,14 +123,14 @@ def test_unaligned_operands_are_refused():
     choice takes the tiled SIMT kernel, exact."""
     A, B = inputs.draw(64, 64, 10, "bf16", "int", seed=9950)
     with pytest.raises(tg.GemmError) as e:
-        tg.matmul(A.cuda(), B.cuda(), kernel="simt_small")
+        tg.matmul(A.cuda(), B.cuda(), kernel="tile16")
     assert e.value.code == tg.binding.ERR_UNSUPPORTED
     A2, B2 = inputs.draw(64, 64, 64, "bf16", "int", seed=9951)
     base = torch.zeros(64 * 64 + 2, dtype=torch.bfloat16, device="cuda")
     dA = base[2:].view(64, 64)
     dA.copy_(A2.cuda())
     with pytest.raises(tg.GemmError) as e:
-        tg.matmul(dA, B2.cuda(), kernel="simt_small")
+        tg.matmul(dA, B2.cuda(), kernel="tile16")
     assert e.value.code == tg.binding.ERR_UNSUPPORTED
     C = tg.matmul(dA, B2.cuda())
     ref, _ = oracle.gemm(A2, B2, nthreads=1)
@@ -145,7 +145,7 @@ def test_named_edge_workload_random_values(in_dt):
     A, B = inputs.draw(96, 200, 1000, in_dt, "normal", seed=9960)
     C_ref, Cabs = oracle.gemm(A, B)
     for out in OUT_TYPES:
-        C = tg.matmul(A.cuda(), B.cuda(), out_dtype=out, kernel="simt_small").cpu()
+        C = tg.matmul(A.cuda(), B.cuda(), out_dtype=out, kernel="tile16").cpu()
         tolerance_check(C, C_ref, Cabs)
 
 
@@ -157,8 +157,8 @@ def test_fp32_random_values_and_run_to_run():
         A, B = inputs.draw(M, N, K, "f32", "normal", seed=seed)
         C_ref, Cabs = oracle.gemm(A, B)
         dA, dB = A.cuda(), B.cuda()
-        C1 = tg.matmul(dA, dB, kernel="simt_small").cpu()
-        C2 = tg.matmul(dA, dB, kernel="simt_small").cpu()
+        C1 = tg.matmul(dA, dB, kernel="tile16").cpu()
+        C2 = tg.matmul(dA, dB, kernel="tile16").cpu()
         tolerance_check(C1, C_ref, Cabs)
         assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
 
@@ -168,11 +168,11 @@ def test_k0_and_beta():
     A = torch.zeros(40, 0, dtype=torch.float16, device="cuda")
     B = torch.zeros(0, 24, dtype=torch.float16, device="cuda")
     C = torch.full((40, 24), float("nan"), device="cuda")
-    tg.addmm(A, B, C, beta=0.0, kernel="simt_small")
+    tg.addmm(A, B, C, beta=0.0, kernel="tile16")
     torch.cuda.synchronize()
     assert not C.any()
     C_in = torch.randint(-5, 6, (40, 24), device="cuda").float()
     C = C_in.clone()
-    tg.addmm(A, B, C, alpha=3.0, beta=2.0, kernel="simt_small")
+    tg.addmm(A, B, C, alpha=3.0, beta=2.0, kernel="tile16")
     torch.cuda.synchronize()
     assert torch.equal(C, 2.0 * C_in)

@@ -35,7 +35,7 @@ KERNELS = {
     "tc_256x256": 5,
     "tc_256x128": 6,
     "tc_small": 7,
-    "simt_small": 8,
+    "tile16": 8,
 }
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 

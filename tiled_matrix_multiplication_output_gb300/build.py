@@ -26,7 +26,7 @@ LIB_NAME = "libtiled_gemm.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 STAMP_PATH = LIB_PATH + ".sha256"
 SOURCES = ("api.cu", "tc_gemm.cu", "tc_gemm_nn.cu", "tc_gemm_tn.cu", "tc_gemm_nt.cu",
-           "tc_gemm_tt.cu", "tc_gemm_splitk.cu", "tc_small.cu", "simt_gemm.cu", "simt_small.cu",
+           "tc_gemm_tt.cu", "tc_gemm_splitk.cu", "tc_small.cu", "simt_gemm.cu", "tile16.cu",
            "model.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -137,20 +137,22 @@ bool small_kernel_fits(int64_t M, int64_t N, int64_t K, int num_sms)
     return tiles <= num_sms && (K + 63) / 64 < kSplitMinKBlocks;
 }
 
-// Whether the latency-path SIMT kernel (simt_small.cu) takes a product.
-// Its 16 x 16 tiles each get a block of their own with the tile's whole K
-// range copied at once, so it is the fastest path while those tiles fit on
-// the SMs in one wave and K is short; for operands the tensor-core kernels
-// cannot take (FP32, or unaligned 16-bit pitches) it also beats the 64 x 64
-// SIMT kernel up to about eight tiles per SM.  Measured on GB300, L2
-// overwritten between calls, microseconds (this kernel / the previous
-// choice / cuBLAS): 128^3 F16 -> F32 6.3-7.0 / 7.9-8.3 (tc_small) /
-// 6.1-6.5; 96 x 200 x 1000 BF16 -> F32 9.7-10.3 / 11.0-11.3 / 8.4;
-// 160 x 160 x 640 BF16 8.4-8.7 / 9.1-9.7; 256^3 BF16 8.4-8.7 / 8.2-8.6
-// (two tiles per SM: not taken); FP32 128^3 7.1 / 12.6 (SIMT) / 9.9;
-// FP32 100 x 200 x 1000 12.6 / 58.0 / 19.0; FP32 512^3 22.4 / 33.4 / 18.6;
-// FP32 768^3 63.8 / 46.9 (nine tiles per SM: not taken).
-bool simt_small_takes(const Problem& q, bool tensor_ok, int num_sms)
+// Whether the latency-path kernel (tile16.cu) takes a product.  Its 16 x 16
+// tiles each get a block with the tile's whole K range copied at once, so
+// it is the fastest path while the blocks' copies are short: one tile per
+// SM up to K = 2048, or up to three tiles per SM with at most 1024 x SMs
+// tile-K values in all.  For operands the tensor-core kernels cannot take
+// (FP32, or unaligned 16-bit rows) it also beats the 64 x 64 SIMT kernel up
+// to eight tiles per SM.  Measured on GB300 with L2 overwritten between
+// calls, microseconds (this kernel / the previous choice / cuBLAS): 128^3
+// F16 -> F32 6.1 / 8.3 (tc_small) / 6.4; 96 x 200 x 1000 BF16 -> F32
+// 8.2 / 11.1 / 8.2; 128 x 128 x 2048 BF16 10.2 / 12.3 (split-K) / 9.2;
+// 256 x 256 x 512 8.1 / 8.8 / 7.1; 320 x 320 x 256 8.2 / 8.6 / 6.2; not
+// taken: 256 x 256 x 1024 10.1 / 9.8, 384 x 384 x 128 8.7 / 8.1, 512^3
+// 12.3 / 8.7.  FP32: 128^3 6.6 / 12.8 (SIMT) / 10.0; 100 x 200 x 1000
+// 12.0 / 59.1 / 19.1; 512^3 21.2 / 33.4 / 18.7; not taken: 768^3 57.6 /
+// 47.1.
+bool tile16_takes(const Problem& q, bool tensor_ok, int num_sms)
 {
     SimtLaunch l{};
     l.in_dtype = q.in_dtype;
@@ -166,16 +168,18 @@ bool simt_small_takes(const Problem& q, bool tensor_ok, int num_sms)
     l.N = static_cast<int>(q.N);
     l.K = static_cast<int>(q.K);
     l.num_sms = num_sms;
-    if (!simt_small_fits(l))
+    if (!tile16_fits(l))
         return false;
     const int64_t tiles = ((q.M + 15) / 16) * ((q.N + 15) / 16);
-    if (tensor_ok)
-        return tiles <= num_sms && q.K <= 1024;
-    return tiles <= int64_t(8) * num_sms;
+    if (!tensor_ok)
+        return tiles <= int64_t(8) * num_sms;
+    if (tiles <= num_sms)
+        return q.K <= 2048;
+    return tiles <= int64_t(3) * num_sms && tiles * q.K <= int64_t(1024) * num_sms;
 }
 
-// The automatic choice.  Small products go to the latency-path SIMT kernel
-// (simt_small_takes); other operands the tensor-core kernels cannot take go
+// The automatic choice.  Small products go to the latency-path kernel
+// (tile16_takes); other operands the tensor-core kernels cannot take go
 // to the tiled SIMT kernel; otherwise the tensor-core variant with the
 // smallest predicted time: the tile traffic of the loop nest, the waves of
 // tiles over the resident CTAs and each tile shape's measured throughput
@@ -184,8 +188,8 @@ int auto_kernel(const Problem& q, int num_sms)
 {
     const int64_t M = q.M, N = q.N, K = q.K;
     const bool tensor_ok = tc_eligible(q);
-    if (simt_small_takes(q, tensor_ok, num_sms))
-        return GEMM_KERNEL_SIMT_SMALL;
+    if (tile16_takes(q, tensor_ok, num_sms))
+        return GEMM_KERNEL_TILE16;
     if (!tensor_ok)
         return GEMM_KERNEL_SIMT;
     const double flops = 2.0 * double(M) * double(N) * double(K);
@@ -233,7 +237,7 @@ int run(const Problem& q, int kernel, cudaStream_t stream)
     int rc = validate_problem(q);
     if (rc != GEMM_OK)
         return rc;
-    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_SIMT_SMALL)
+    if (kernel < GEMM_KERNEL_AUTO || kernel > GEMM_KERNEL_TILE16)
         return GEMM_ERR_INVALID_VALUE;
     if (q.M == 0 || q.N == 0)
         return GEMM_OK;
@@ -284,7 +288,7 @@ int run(const Problem& q, int kernel, cudaStream_t stream)
     l.N = static_cast<int>(q.N);
     l.K = static_cast<int>(q.K);
     l.num_sms = d.num_sms;
-    cudaError_t err = (kernel == GEMM_KERNEL_SIMT_SMALL) ? simt_small_launch(l, stream)
+    cudaError_t err = (kernel == GEMM_KERNEL_TILE16) ? tile16_launch(l, stream)
                                                          : simt_gemm_launch(l, stream);
     if (err == cudaErrorNotSupported)
         return GEMM_ERR_UNSUPPORTED;

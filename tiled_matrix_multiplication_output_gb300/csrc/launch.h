@@ -34,14 +34,14 @@ struct SimtLaunch {
 
 cudaError_t simt_gemm_launch(const SimtLaunch& l, cudaStream_t stream);
 
-// The latency-path SIMT kernel (simt_small.cu): one 16 x 16 output tile per
-// block, the tile's whole K range copied at once and split between the
-// block's warps.  simt_small_fits says whether it takes the operands
+// The latency-path kernel (tile16.cu): one 16 x 16 output tile per block,
+// the tile's whole K range copied at once and split between the block's
+// warps (warp-level MMA for 16-bit inputs, FFMA for FP32).  tile16_fits says whether it takes the operands
 // (16-byte aligned A and B and row pitches, the K slices of a tile within
-// a block's shared memory); simt_small_launch returns cudaErrorNotSupported
+// a block's shared memory); tile16_launch returns cudaErrorNotSupported
 // when it does not.
-bool simt_small_fits(const SimtLaunch& l);
-cudaError_t simt_small_launch(const SimtLaunch& l, cudaStream_t stream);
+bool tile16_fits(const SimtLaunch& l);
+cudaError_t tile16_launch(const SimtLaunch& l, cudaStream_t stream);
 
 struct TcLaunch {
     int variant;        // TC_128x128, TC_128x256 or TC_256x256
