@@ -521,8 +521,11 @@ def small_workload_lines(dev, flush_buf_bytes):
         _, per = timed_loop(step, 400, stream, flush)
         gpu_us = statistics.median(per) * 1e3
         gpu_us_mean = trimmed_mean(per) * 1e3
+        chosen = tg.gemm_select_kernel(A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K,
+                                       in_code, tg.F32, out_code)
         line = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "in_dtype": w.in_dtype,
-                "out_dtype": w.out_dtype, "gpu_us": gpu_us, "gpu_us_trimmed_mean": gpu_us_mean,
+                "out_dtype": w.out_dtype, "kernel": tg.KERNEL_NAMES.get(chosen, str(chosen)),
+                "gpu_us": gpu_us, "gpu_us_trimmed_mean": gpu_us_mean,
                 "gpu_tflops": w.flops / (gpu_us * 1e-6) / 1e12,
                 "gpu_gbs_compulsory": footprint_bytes(w) / (gpu_us * 1e-6) / 1e9}
         if w.in_dtype != "f32":
