@@ -70,6 +70,11 @@ def parse_args():
                     help="instead of the benchmark line: time the extended forms (transposed "
                          "operands, alpha/beta, split-K, last-wave split) on fixed BF16 "
                          "problems, one JSON line each")
+    ap.add_argument("--small-sweep", action="store_true",
+                    help="instead of the benchmark line: time the small-product kernels "
+                         "(tile16, tc_small, tc_128x128, the SIMT kernel), the automatic choice "
+                         "and cuBLAS on a fixed list of small shapes with L2 overwritten "
+                         "between calls, one JSON line per shape")
     ap.add_argument("--simt", action="store_true",
                     help="instead of the benchmark line: time the SIMT kernel on FP32 and "
                          "unaligned 16-bit products in every operand layout, one JSON line each")
@@ -780,6 +785,66 @@ def run_sweep():
         print(json.dumps(row), flush=True)
 
 
+SMALL_SWEEP_SHAPES = [
+    ("bf16", "bf16", 64, 64, 64), ("bf16", "bf16", 128, 128, 128), ("bf16", "bf16", 96, 200, 1000),
+    ("bf16", "bf16", 128, 128, 1024), ("bf16", "bf16", 192, 192, 192), ("bf16", "bf16", 256, 256, 256),
+    ("bf16", "bf16", 256, 128, 512), ("bf16", "bf16", 64, 64, 2048), ("bf16", "bf16", 128, 128, 2048),
+    ("bf16", "bf16", 32, 1024, 256), ("bf16", "bf16", 256, 256, 512), ("bf16", "bf16", 384, 384, 128),
+    ("bf16", "bf16", 512, 512, 128), ("bf16", "bf16", 128, 128, 512), ("bf16", "bf16", 160, 160, 640),
+    ("bf16", "bf16", 256, 256, 1024), ("bf16", "bf16", 192, 192, 1024), ("bf16", "bf16", 320, 320, 256),
+    ("bf16", "bf16", 384, 384, 384), ("bf16", "bf16", 512, 512, 512), ("bf16", "bf16", 64, 1024, 1024),
+    ("f16", "f32", 128, 128, 128), ("bf16", "f32", 96, 200, 1000),
+    ("f32", "f32", 128, 128, 128), ("f32", "f32", 100, 200, 1000), ("f32", "f32", 512, 512, 512),
+    ("f32", "f32", 640, 640, 640), ("f32", "f32", 768, 768, 768)]
+
+
+def run_small_sweep():
+    """Per-call GPU time (microseconds, trimmed mean of 300 calls with L2
+    overwritten between them, outside the events) of each small-product
+    kernel forced, of the automatic choice through gemm_ex_ws, and of
+    cuBLAS (torch.matmul, TF32 off) on N(0, 1) inputs."""
+    import torch
+    import tiled_matrix_multiplication_output_gb300 as tg
+    tg.load_library(build_if_missing=True)
+    torch.cuda.set_device(0)
+    torch.backends.cuda.matmul.allow_tf32 = False
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev)
+    dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+    g = torch.Generator(device="cuda").manual_seed(0)
+
+    def us(fn):
+        for _ in range(5):
+            fn()
+        _, per = timed_loop(fn, 300, stream, flush)
+        return round(trimmed_mean(per) * 1e3, 2)
+
+    for in_dt, out_dt, M, N, K in SMALL_SWEEP_SHAPES:
+        A = torch.randn(M, K, device=dev, generator=g).to(dt[in_dt])
+        B = torch.randn(K, N, device=dev, generator=g).to(dt[in_dt])
+        C = torch.empty(M, N, device=dev, dtype=dt[out_dt])
+        ic, oc = tg.binding.dtype_code(dt[in_dt]), tg.binding.dtype_code(dt[out_dt])
+        row = {"shape": [M, N, K], "in": in_dt, "out": out_dt}
+        kernels = ("tile16", "simt") if in_dt == "f32" else ("tile16", "tc_small", "tc_128x128", "simt")
+        for k in kernels:
+            kid = tg.KERNELS[k]
+            row[k] = us(lambda: tg.gemm_ex_kernel(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                                  ic, tg.F32, oc, kid, stream.cuda_stream))
+        ws_bytes = max(16, tg.gemm_workspace_size(M, N, K))
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        row["auto"] = us(lambda: tg.gemm_ex_ws(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, ic,
+                                               tg.F32, oc, ws.data_ptr(), ws_bytes,
+                                               stream.cuda_stream))
+        row["auto_pick"] = tg.KERNEL_NAMES[tg.gemm_select_kernel(
+            A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, ic, tg.F32, oc)]
+        row["cublas"] = us(lambda: torch.matmul(A, B))
+        rc = tg.gemm_device_status(stream.cuda_stream)
+        if rc != 0:
+            raise tg.GemmError(rc, "small sweep")
+        print(json.dumps(row), flush=True)
+
+
 SIMT_SHAPES = [("f32", 4096, 4096, 4096), ("f32", 8192, 8192, 1024), ("f32", 2048, 2048, 2048),
                ("bf16", 4095, 4095, 4095)]
 
@@ -897,6 +962,9 @@ def main():
         return
     if args.simt:
         run_simt()
+        return
+    if args.small_sweep:
+        run_small_sweep()
         return
     world_env = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
