@@ -75,6 +75,11 @@ def parse_args():
                          "(tile16, tc_small, tc_128x128, the SIMT kernel), the automatic choice "
                          "and cuBLAS on a fixed list of small shapes with L2 overwritten "
                          "between calls, one JSON line per shape")
+    ap.add_argument("--sweep-shapes", default="",
+                    help="with --small-sweep: a comma-separated list of MxNxK BF16 shapes "
+                         "(BF16 output) instead of the fixed list")
+    ap.add_argument("--sweep-calls", type=int, default=300,
+                    help="with --small-sweep: timed calls per entry")
     ap.add_argument("--simt", action="store_true",
                     help="instead of the benchmark line: time the SIMT kernel on FP32 and "
                          "unaligned 16-bit products in every operand layout, one JSON line each")
@@ -798,8 +803,8 @@ SMALL_SWEEP_SHAPES = [
     ("f32", "f32", 640, 640, 640), ("f32", "f32", 768, 768, 768)]
 
 
-def run_small_sweep():
-    """Per-call GPU time (microseconds, trimmed mean of 300 calls with L2
+def run_small_sweep(shapes_arg="", calls=300):
+    """Per-call GPU time (microseconds, trimmed mean of `calls` calls with L2
     overwritten between them, outside the events) of each small-product
     kernel forced, of the automatic choice through gemm_ex_ws, and of
     cuBLAS (torch.matmul, TF32 off) on N(0, 1) inputs."""
@@ -815,12 +820,16 @@ def run_small_sweep():
     g = torch.Generator(device="cuda").manual_seed(0)
 
     def us(fn):
-        for _ in range(5):
+        for _ in range(min(5, calls)):
             fn()
-        _, per = timed_loop(fn, 300, stream, flush)
+        _, per = timed_loop(fn, max(1, calls), stream, flush)
         return round(trimmed_mean(per) * 1e3, 2)
 
-    for in_dt, out_dt, M, N, K in SMALL_SWEEP_SHAPES:
+    shapes = SMALL_SWEEP_SHAPES
+    if shapes_arg:
+        shapes = [("bf16", "bf16") + tuple(int(x) for x in item.split("x"))
+                  for item in shapes_arg.split(",")]
+    for in_dt, out_dt, M, N, K in shapes:
         A = torch.randn(M, K, device=dev, generator=g).to(dt[in_dt])
         B = torch.randn(K, N, device=dev, generator=g).to(dt[in_dt])
         C = torch.empty(M, N, device=dev, dtype=dt[out_dt])
@@ -964,7 +973,7 @@ def main():
         run_simt()
         return
     if args.small_sweep:
-        run_small_sweep()
+        run_small_sweep(args.sweep_shapes, args.sweep_calls)
         return
     world_env = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
