@@ -176,3 +176,22 @@ def test_k0_and_beta():
     tg.addmm(A, B, C, alpha=3.0, beta=2.0, kernel="tile16")
     torch.cuda.synchronize()
     assert torch.equal(C, 2.0 * C_in)
+
+
+@pytest.mark.parametrize("in_dt", ["f32", "bf16"])
+@pytest.mark.parametrize("op_a,op_b", OPS)
+def test_addmm_every_layout_and_output(in_dt, op_a, op_b):
+    """C = 2 op(A) op(B) - C_in on tile16 with integer inputs and an integer
+    C_in: exact in every output type (values stay below 2^11), every
+    layout, FP32 and BF16 inputs; ragged 136 x 200 x 72."""
+    M, N, K = 136, 200, 72
+    A0, B0 = inputs.draw(M, N, K, in_dt, "int", lo=-2, hi=2, seed=9990)
+    A, B = _stored(A0, B0, op_a, op_b)
+    for j, out in enumerate(OUT_TYPES):
+        C_in = torch.randint(-50, 51, (M, N), generator=torch.Generator().manual_seed(9991 + j)).to(out)
+        C = tg.addmm(A.cuda(), B.cuda(), C_in.cuda(), op_a=op_a, op_b=op_b, alpha=2.0, beta=-1.0,
+                     kernel="tile16").cpu()
+        ref, _ = oracle.gemm_general(A, B, op_a, op_b, alpha=2.0, beta=-1.0, C_in=C_in)
+        np.testing.assert_array_equal(C.double().numpy(),
+                                      oracle.round_to(ref, out).double().numpy(),
+                                      err_msg=f"{in_dt} {op_a}{op_b} -> {out}")
