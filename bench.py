@@ -803,6 +803,20 @@ SMALL_SWEEP_SHAPES = [
     ("f32", "f32", 640, 640, 640), ("f32", "f32", 768, 768, 768)]
 
 
+def parse_sweep_shapes(arg):
+    """'MxNxK,MxNxK,...' -> [("bf16", "bf16", M, N, K), ...]; empty -> the
+    fixed list.  Sizes must be positive integers."""
+    if not arg:
+        return list(SMALL_SWEEP_SHAPES)
+    shapes = []
+    for item in arg.split(","):
+        dims = item.strip().lower().split("x")
+        if len(dims) != 3 or not all(d.isdigit() and int(d) > 0 for d in dims):
+            raise ValueError(f"bad shape {item!r}: want MxNxK with positive sizes")
+        shapes.append(("bf16", "bf16") + tuple(int(d) for d in dims))
+    return shapes
+
+
 def run_small_sweep(shapes_arg="", calls=300):
     """Per-call GPU time (microseconds, trimmed mean of `calls` calls with L2
     overwritten between them, outside the events) of each small-product
@@ -825,11 +839,7 @@ def run_small_sweep(shapes_arg="", calls=300):
         _, per = timed_loop(fn, max(1, calls), stream, flush)
         return round(trimmed_mean(per) * 1e3, 2)
 
-    shapes = SMALL_SWEEP_SHAPES
-    if shapes_arg:
-        shapes = [("bf16", "bf16") + tuple(int(x) for x in item.split("x"))
-                  for item in shapes_arg.split(",")]
-    for in_dt, out_dt, M, N, K in shapes:
+    for in_dt, out_dt, M, N, K in parse_sweep_shapes(shapes_arg):
         A = torch.randn(M, K, device=dev, generator=g).to(dt[in_dt])
         B = torch.randn(K, N, device=dev, generator=g).to(dt[in_dt])
         C = torch.empty(M, N, device=dev, dtype=dt[out_dt])

@@ -166,3 +166,12 @@ def test_roofline_carries_the_theoretical_tensor_peak():
 def test_trimmed_mean_drops_the_tails():
     assert bench.trimmed_mean([1.0] * 8 + [100.0, -50.0]) == pytest.approx(1.0)
     assert bench.trimmed_mean([2.0, 4.0]) == pytest.approx(3.0)
+
+
+def test_parse_sweep_shapes():
+    assert bench.parse_sweep_shapes("") == list(bench.SMALL_SWEEP_SHAPES)
+    assert bench.parse_sweep_shapes("256x128x64, 8X8X8") == [("bf16", "bf16", 256, 128, 64),
+                                                            ("bf16", "bf16", 8, 8, 8)]
+    for bad in ("256x128", "0x8x8", "8x8x-1", "axbxc", "8x8x8,"):
+        with pytest.raises(ValueError):
+            bench.parse_sweep_shapes(bad)
