@@ -343,7 +343,7 @@ def test_automatic_choice_on_the_named_workloads():
     """The automatic picks on the named workloads: the latency-path kernel
     when its 16 x 16 tiles' copies are short (one tile per SM up to K =
     2048, or up to three per SM and 1024 x SMs tile-K values; aligned FP32
-    products of up to eight tiles per SM), the non-persistent
+    products of up to eleven tiles per SM), the non-persistent
     single-tile kernel when 128 x 64 tiles fit in one wave, the CTA-pair
     kernel for the large squares, the tiled SIMT kernel for the rest of FP32
     and for shapes the tensor maps cannot take."""
@@ -357,6 +357,8 @@ def test_automatic_choice_on_the_named_workloads():
     assert pick(128, 128, 128, tg.F16, tg.F32, torch.float16) == "tile16"
     assert pick(96, 200, 1000, tg.BF16, tg.F32) == "tile16"
     assert pick(100, 200, 1000, tg.F32, tg.F32, torch.float32) == "tile16"
+    assert pick(640, 640, 640, tg.F32, tg.F32, torch.float32) == "tile16"     # 10.5 tiles per SM
+    assert pick(768, 768, 768, tg.F32, tg.F32, torch.float32) == "simt"       # 15.2 tiles per SM
     assert pick(1024, 1024, 1024, tg.F32, tg.F32, torch.float32) == "simt"
     assert pick(256, 256, 256, tg.BF16, tg.BF16) == "tile16"      # two tiles per SM, short K
     assert pick(128, 128, 2048, tg.BF16, tg.BF16) == "tile16"

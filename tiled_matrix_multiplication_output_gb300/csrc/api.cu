@@ -142,16 +142,17 @@ bool small_kernel_fits(int64_t M, int64_t N, int64_t K, int num_sms)
 // it is the fastest path while the blocks' copies are short: one tile per
 // SM up to K = 2048, or up to three tiles per SM with at most 1024 x SMs
 // tile-K values in all.  For operands the tensor-core kernels cannot take
-// (FP32, or unaligned 16-bit rows) it also beats the 64 x 64 SIMT kernel up
-// to eight tiles per SM.  Measured on GB300 with L2 overwritten between
+// (FP32, or unaligned 16-bit rows) it also beats the tiled SIMT kernel up
+// to eleven tiles per SM.  Measured on GB300 with L2 overwritten between
 // calls, microseconds (this kernel / the previous choice / cuBLAS): 128^3
 // F16 -> F32 6.1 / 8.3 (tc_small) / 6.4; 96 x 200 x 1000 BF16 -> F32
 // 8.2 / 11.1 / 8.2; 128 x 128 x 2048 BF16 10.2 / 12.3 (split-K) / 9.2;
 // 256 x 256 x 512 8.1 / 8.8 / 7.1; 320 x 320 x 256 8.2 / 8.6 / 6.2; not
 // taken: 256 x 256 x 1024 10.1 / 9.8, 384 x 384 x 128 8.7 / 8.1, 512^3
 // 12.3 / 8.7.  FP32: 128^3 6.6 / 12.8 (SIMT) / 10.0; 100 x 200 x 1000
-// 12.0 / 59.1 / 19.1; 512^3 21.2 / 33.4 / 18.7; not taken: 768^3 57.6 /
-// 47.1.
+// 12.0 / 59.1 / 19.1; 512^3 21.2 / 33.4 / 18.7; 640^3 (10.5 tiles per SM)
+// 37.4-37.6 / 39.3-39.8 / 22.6; not taken: 768^3 (15 per SM) 57.6-57.9 /
+// 46.9-47.1.
 bool tile16_takes(const Problem& q, bool tensor_ok, int num_sms)
 {
     SimtLaunch l{};
@@ -172,7 +173,7 @@ bool tile16_takes(const Problem& q, bool tensor_ok, int num_sms)
         return false;
     const int64_t tiles = ((q.M + 15) / 16) * ((q.N + 15) / 16);
     if (!tensor_ok)
-        return tiles <= int64_t(8) * num_sms;
+        return tiles <= int64_t(11) * num_sms;
     if (tiles <= num_sms)
         return q.K <= 2048;
     return tiles <= int64_t(3) * num_sms && tiles * q.K <= int64_t(1024) * num_sms;
